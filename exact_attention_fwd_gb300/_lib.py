@@ -1,0 +1,73 @@
+"""ctypes binding of libfa.so: the C ABI of include/fa.h under the same names.
+
+Argument marshalling only.  Every step of the computation runs in the
+library's CUDA kernels; nothing here computes attention, and there is no
+fallback: if libfa.so is missing the calls raise.
+"""
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F16 = range(3)
+
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_sync_status", "fa_status_string")
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def load():
+    """Load libfa.so (once) and declare the signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is not built; run exact_attention_fwd_gb300.build.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp, sz, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_sync_status.argtypes = [vp]
+    lib.fa_sync_status.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(s):
+    return load().fa_status_string(int(s)).decode()
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream):
+    """Raw call: pointers are ints (device addresses); returns the status."""
+    return load().fa_fwd(q, k, v, o, lse, B, H, N, d, float(scale), int(causal), int(dtype),
+                         stream)
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, dtype, grad_dtype,
+           workspace, workspace_bytes, stream):
+    return load().fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, float(scale), int(causal),
+                         int(dtype), int(grad_dtype), workspace, workspace_bytes, stream)
+
+
+def fa_bwd_workspace_size(B, H, N):
+    return int(load().fa_bwd_workspace_size(B, H, N))
+
+
+def fa_sync_status(stream):
+    return load().fa_sync_status(stream)

@@ -1,0 +1,86 @@
+"""torch-tensor front end of the C ABI (argument marshalling only).
+
+torch supplies device memory and the current stream; the library's kernels do
+all the work.  Errors from the library raise _lib.FaError.
+"""
+
+import math
+
+import torch
+
+from . import _lib
+
+_DTYPES = {torch.float32: _lib.FA_DTYPE_F32, torch.bfloat16: _lib.FA_DTYPE_BF16}
+
+
+def _check(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _stream_handle(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+    """O, LSE = attention(q, k, v).  q, k, v: [B, N, H, d] float32 or bfloat16."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, q.dtype)
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise ValueError("q, k, v must share one [B, N, H, d] shape")
+    B, N, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check(out, "out", q.dtype)
+    _check(lse, "lse", torch.float32)
+    st = _lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                     B, H, N, d, scale, causal, _DTYPES[q.dtype], _stream_handle(stream))
+    if st != _lib.FA_OK:
+        raise _lib.FaError(st, "fa_fwd")
+    return out, lse
+
+
+def workspace(B, H, N, device):
+    """A device workspace tensor sized for fa_bwd."""
+    n = _lib.fa_bwd_workspace_size(B, H, N)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def backward(q, k, v, o, lse, do, scale=None, causal=False, grad_dtype=None, ws=None,
+             dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV of attention given the forward's O and LSE and the incoming dO."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check(t, name, q.dtype)
+    _check(lse, "lse", torch.float32)
+    B, N, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    gdt = q.dtype if grad_dtype is None else grad_dtype
+    if ws is None:
+        ws = workspace(B, H, N, q.device)
+    dq = torch.empty(q.shape, dtype=gdt, device=q.device) if dq is None else dq
+    dk = torch.empty(q.shape, dtype=gdt, device=q.device) if dk is None else dk
+    dv = torch.empty(q.shape, dtype=gdt, device=q.device) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check(t, name, gdt)
+    st = _lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale,
+                     causal, _DTYPES[q.dtype], _DTYPES[gdt], ws.data_ptr(), ws.numel(),
+                     _stream_handle(stream))
+    if st != _lib.FA_OK:
+        raise _lib.FaError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def sync_status(stream=None):
+    """Synchronise and return (and clear) the device status word."""
+    return _lib.fa_sync_status(_stream_handle(stream))

@@ -1,0 +1,192 @@
+// fa_api.cu — the C ABI declared in include/fa.h: argument validation, the
+// device status word, and dispatch to the float32 SIMT kernels or the bf16
+// tcgen05 kernels.  No call here allocates device memory.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "fa_common.cuh"
+
+namespace {
+
+// One status word per device; kernels record FA_ERR_TIMEOUT here.
+__device__ int g_fa_status = 0;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+// Device address of this device's status word (looked up once per device,
+// with that device current).
+int* status_word(fa_status* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = FA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fa_status) != cudaSuccess) {
+      *err = FA_ERR_CUDA;
+      return nullptr;
+    }
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+  }
+  return g_status_ptr[dev];
+}
+
+bool probe_timeout_requested() {
+  const char* v = std::getenv("FA_SELFTEST_WAIT_TIMEOUT");
+  return v != nullptr && v[0] == '1';
+}
+
+size_t elt_size(fa_dtype t) { return t == FA_DTYPE_F32 ? 4 : 2; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// [a, a + na) and [b, b + nb) overlap
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+fa_status check_shape(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (d < 1 || d % 8 != 0) return FA_ERR_INVALID_ARG;
+  if (d > 128) return FA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  // element count and byte strides must stay far inside 64-bit / TMA limits
+  const long double elems = static_cast<long double>(B) * N * H * d;
+  if (elems * 4 >= static_cast<long double>(1ULL << 40)) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  const size_t bytes = static_cast<size_t>(B) * H * N * sizeof(float);
+  return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, fa_dtype dtype, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (dtype == FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  const size_t tbytes = static_cast<size_t>(B) * N * H * d * elt_size(dtype);
+  const size_t lbytes = static_cast<size_t>(B) * H * N * sizeof(float);
+  for (const void* in : {q, k, v}) {
+    if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes))
+      return FA_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
+
+  fa_status err = FA_OK;
+  int* status = status_word(&err);
+  if (status == nullptr) return err;
+
+  fa::FwdParams p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+  p.B = B; p.H = H; p.N = N; p.d = d;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status;
+  p.probe_timeout = probe_timeout_requested() ? 1 : 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = (dtype == FA_DTYPE_F32) ? fa::launch_fwd_simt_f32(p, s, causal != 0)
+                                          : fa::launch_fwd_tc_bf16(p, s, causal != 0);
+  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, fa_dtype grad_dtype, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  if (dtype == FA_DTYPE_F16 || grad_dtype == FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (grad_dtype != dtype && grad_dtype != FA_DTYPE_F32) return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (workspace_bytes < fa_bwd_workspace_size(B, H, N)) return FA_ERR_INVALID_ARG;
+  for (const void* ptr : {q, k, v, o, dO, static_cast<const void*>(dq),
+                          static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    if (!aligned(ptr, 16)) return FA_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !aligned(workspace, 256)) return FA_ERR_INVALID_ARG;
+  const size_t in_bytes = static_cast<size_t>(B) * N * H * d * elt_size(dtype);
+  const size_t g_bytes = static_cast<size_t>(B) * N * H * d * elt_size(grad_dtype);
+  const size_t l_bytes = static_cast<size_t>(B) * H * N * sizeof(float);
+  const void* outs[] = {dq, dk, dv};
+  const void* ins[] = {q, k, v, o, dO};
+  for (const void* out : outs) {
+    for (const void* in : ins)
+      if (overlaps(out, g_bytes, in, in_bytes)) return FA_ERR_INVALID_ARG;
+    if (overlaps(out, g_bytes, lse, l_bytes) || overlaps(out, g_bytes, workspace, workspace_bytes))
+      return FA_ERR_INVALID_ARG;
+  }
+  if (overlaps(dq, g_bytes, dk, g_bytes) || overlaps(dq, g_bytes, dv, g_bytes) ||
+      overlaps(dk, g_bytes, dv, g_bytes))
+    return FA_ERR_INVALID_ARG;
+  for (const void* in : ins)
+    if (overlaps(workspace, workspace_bytes, in, in_bytes)) return FA_ERR_INVALID_ARG;
+  if (overlaps(workspace, workspace_bytes, lse, l_bytes)) return FA_ERR_INVALID_ARG;
+
+  fa_status err = FA_OK;
+  int* status = status_word(&err);
+  if (status == nullptr) return err;
+
+  fa::BwdParams p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.dO = dO;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.D = static_cast<float*>(workspace);
+  p.B = B; p.H = H; p.N = N; p.d = d;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.grad_f32 = (grad_dtype == FA_DTYPE_F32) ? 1 : 0;
+  p.status = status;
+  p.probe_timeout = probe_timeout_requested() ? 1 : 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_bwd_dot(p, dtype == FA_DTYPE_BF16, s);
+  if (e == cudaSuccess)
+    e = (dtype == FA_DTYPE_F32) ? fa::launch_bwd_simt_f32(p, s, causal != 0)
+                                : fa::launch_bwd_tc_bf16(p, s, causal != 0);
+  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_sync_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return static_cast<fa_status>(v);
+}
+
+}  // extern "C"

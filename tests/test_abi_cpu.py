@@ -1,0 +1,85 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads,
+exports every function include/fa.h declares, and rejects invalid arguments
+before launching anything."""
+
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_fwd_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert {"fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string",
+            "fa_sync_status"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from exact_attention_fwd_gb300 import _lib
+    assert _lib.status_string(0) == "FA_OK"
+    assert _lib.status_string(4) == "FA_ERR_TIMEOUT"
+    assert _lib.status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    from exact_attention_fwd_gb300 import _lib
+    assert _lib.fa_bwd_workspace_size(64, 16, 1024) == 64 * 16 * 1024 * 4
+    assert _lib.fa_bwd_workspace_size(1, 1, 3) == 256
+    assert _lib.fa_bwd_workspace_size(0, 1, 3) == 0
+
+
+FAKE = 1 << 20   # 16-byte aligned address; validation fails before any use
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), 1),                        # null pointer
+    (dict(N=0), 1), (dict(B=-1), 1), (dict(H=0), 1),
+    (dict(d=12), 1), (dict(d=0), 1),       # not a multiple of 8
+    (dict(d=136), 2),                      # above 128
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(dtype=2), 2),                    # fp16 reserved
+    (dict(dtype=7), 1),
+    (dict(q=FAKE + 8), 1),                 # misaligned
+    (dict(o=FAKE), 1),                     # output aliases q
+])
+def test_fwd_rejects_invalid_arguments(lib, kw, want):
+    from exact_attention_fwd_gb300 import _lib
+    a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, B=1, H=1, N=16, d=64,
+             scale=0.125, causal=1, dtype=1, stream=None)
+    a.update(kw)
+    assert _lib.fa_fwd(**a) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(workspace=0), 1),
+    (dict(workspace_bytes=100), 1),
+    (dict(grad_dtype=1, dtype=0), 1),      # bf16 grads of fp32 inputs
+    (dict(dq=FAKE), 1),                    # aliases q
+    (dict(dk=8 * FAKE), 1),                # aliases dq
+    (dict(workspace=FAKE + 16), 1),        # not 256-byte aligned (and aliases)
+])
+def test_bwd_rejects_invalid_arguments(lib, kw, want):
+    from exact_attention_fwd_gb300 import _lib
+    a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, dO=6 * FAKE,
+             dq=8 * FAKE, dk=10 * FAKE, dv=12 * FAKE, B=1, H=1, N=16, d=64, scale=0.125,
+             causal=1, dtype=1, grad_dtype=1, workspace=14 * FAKE, workspace_bytes=4096,
+             stream=None)
+    a.update(kw)
+    assert _lib.fa_bwd(**a) == want
