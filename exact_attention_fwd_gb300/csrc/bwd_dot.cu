@@ -41,8 +41,8 @@ __device__ __forceinline__ float dot_chunk(const uint4& a, const uint4& b, bool 
 
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreads) dot_do_o_kernel(BwdParams p) {
-  // partial sums of one warp's rows: at most 32 rows x 16 chunks
-  __shared__ float part[kThreads / 32][kRowsPerWarp * 16];
+  // partial sums of one warp's rows: 32 rows x at most 32 chunks (fp32, d = 128)
+  __shared__ float part[kThreads / 32][kRowsPerWarp * 32];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int elt = kBf16 ? 2 : 4;
   const int cpr = p.d * elt / 16;                       // 16-byte chunks per row

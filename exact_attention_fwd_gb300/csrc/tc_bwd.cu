@@ -1,9 +1,614 @@
-// tc_bwd.cu — bf16 attention backward on the sm_103a tensor cores (pending).
+// tc_bwd.cu — bf16 attention backward on the sm_103a tensor cores.
+//
+// Algorithm: "Flash Attention 2 — backward pass notes", section "The math (FA2
+// backward with recompute)": with the saved L, P = exp(S - L) is recomputed;
+// dP = dO V^T, dS = P (dP - D) with D = <dO, O>, dV = P^T dO,
+// dK = scale dS^T Q, dQ = scale dS K.  Split as the same page's option 3 ("Why
+// the WGSL kernel isn't shipped this turn"): one kernel whose CTA owns a tile
+// of queries and accumulates dQ, one whose CTA owns a tile of keys and
+// accumulates dK and dV.  Each output row is written once, by one CTA: no
+// float atomics.  Rows whose L is -inf contribute nothing ("Caveats specific
+// to the backward path").
+//
+// Precision.  The forward stores O in bf16, and D computed from that O (the
+// pre-pass, bwd_dot.cu) is off by up to |dO| |O| 2^-9 per row; the gradient
+// amplifies that by |K| scale, which exceeds the bf16 gradient tolerance when
+// Q and K have large entries.  The dQ kernel therefore also accumulates the
+// exact-form D_i = sum_j P_ij dP_ij in fp32 and B_i = sum_j P_ij K_j, runs its
+// loop with the pre-pass value D~ and adds scale (D~_i - D_i) B_i at the end
+// (algebraically the same dQ); it writes the refined D back to the workspace,
+// and the dK/dV kernel, launched after it, uses that.  dS (and P for B) are
+// staged for the tensor cores in fp16, whose 11-bit significand keeps the
+// product error ~8x below bf16's; the streamed K or Q tile they multiply is
+// converted to an fp16 copy in shared memory (an MMA takes one input type).
+// This bounds |Q|, |K| and |dS| by fp16's range (65504) in the backward.
+//
+// Both kernels share one skeleton (template parameter kDkDv):
+//   row tile   : the CTA's 128 rows, resident in shared memory for the whole
+//                kernel.  dQ kernel: Q and dO of 128 queries.  dK/dV kernel: K
+//                and V of 128 keys.
+//   loop block : 64 rows streamed through a TMA ring.  dQ: K_j and V_j of 64
+//                keys.  dK/dV: Q_i and dO_i of 64 queries (plus their L, D).
+//   per block  : S = R1 C1^T and dP = R2 C2^T (tcgen05, M=128, N=64, K=d, bf16,
+//                both operands K-major); one thread per row forms P and dS and
+//                writes them back to TMEM (P in S's columns, dS in dP's); then
+//                dQ kernel:    dQ += dS K_j, B += P K_j      (fp16)
+//                dK/dV kernel: dV += P dO_i (bf16), dK += dS Q_i (fp16)
+//                with A read from TMEM and B the streamed tile as an MN-major
+//                operand.
+//   S and dP are double-buffered in TMEM and two element-wise warpgroups take
+//   alternate blocks, so one block's exponentials overlap the other block's
+//   MMAs.
+//
+// Roles (12 warps): warp 0 TMA producer, warp 1 MMA issuer, warp 2 loads the
+// per-query L and D of each block (dK/dV kernel), warp 3 converts the streamed
+// C1 tile to fp16, warps 4-7 and 8-11 are the element-wise warpgroups (and the
+// epilogue: each stores half of the columns of the accumulator rows).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+
 #include "fa_common.cuh"
+#include "sm103_ptx.cuh"
+#include "tmap.h"
 
 namespace fa {
+namespace {
 
-cudaError_t launch_bwd_tc_bf16(const BwdParams&, cudaStream_t, bool) {
+constexpr int kRows = 128;       // rows owned by a CTA
+constexpr int kBlk = 64;         // rows of one streamed block
+constexpr int kThreads = 384;
+constexpr int kTmemCols = 512;
+constexpr int kMaxStages = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int DP>
+struct BwdCfg {
+  static constexpr int kStages = (DP == 64) ? 4 : 3;
+  static constexpr int kChunks = DP / 64;
+  static constexpr int kRowChunk = kRows * 128;          // 16 KB: 128 rows x 64 cols
+  static constexpr int kBlkChunk = kBlk * 128;           // 8 KB: 64 rows x 64 cols
+  static constexpr int kRowTile = kChunks * kRowChunk;
+  static constexpr int kBlkTile = kChunks * kBlkChunk;
+  static constexpr int kVecBytes = 1024;                 // L2 and D of 64 queries (512 B),
+                                                         // padded to keep stages 1 KB aligned
+  // stage: C1 (bf16) | C2 (bf16) | C1 as fp16 | vectors
+  static constexpr int kStageBytes = 3 * kBlkTile + kVecBytes;
+  static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
+  static constexpr int kR1Off = 0;
+  static constexpr int kR2Off = kRowTile;
+  static constexpr int kStageOff = 2 * kRowTile;
+  static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kDsumOff = kBarOff + 512;         // 2 x 128 floats
+  static constexpr int kSmemBytes = kDsumOff + 1024 + 1024;
+  // TMEM columns
+  static constexpr int kTS = 0;            // S buffers: kTS + b * 64 (P written over S)
+  static constexpr int kTdP = 128;         // dP buffers: kTdP + b * 64 (dS written over dP)
+  static constexpr int kTAcc1 = 256;       // dV (dK/dV kernel) or B (dQ kernel)
+  static constexpr int kTAcc2 = 256 + DP;  // dK or dQ
+};
+
+struct BwdBars {
+  uint64_t r_full;
+  uint64_t c_full[kMaxStages];
+  uint64_t c_empty[kMaxStages];
+  uint64_t vec_full[kMaxStages];
+  uint64_t conv_full[kMaxStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t acc_full;
+  uint64_t dsum;
+  uint64_t drain;
+  uint64_t probe;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(BwdBars) <= 512, "barrier block");
+
+__device__ __forceinline__ void raise_abort(BwdBars* bars, int* status) {
+  record_error(status, FA_ERR_TIMEOUT);
+  *reinterpret_cast<volatile int*>(&bars->abort) = 1;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* ab,
+                                          long long budget) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, budget));
+}
+
+// Store 32-column groups [col0, col0 + ncols) of this thread's accumulator row
+// at TMEM address `acc`, as mult * (acc + corr * acc_b) (acc_b read only when
+// kCorr), to a row of d elements of type float or bf16.
+template <bool kF32, bool kCorr>
+__device__ __forceinline__ void store_acc_cols(uint32_t acc, uint32_t acc_b, float corr, int col0,
+                                               int ncols, float mult, void* row_ptr, int d,
+                                               bool store) {
+  for (int cc = col0; cc < col0 + ncols; cc += 32) {
+    uint32_t r[32];
+    tmem_ld32(acc + cc, r);
+    tmem_ld_wait(r);
+    if (kCorr) {
+      uint32_t rb[32];
+      tmem_ld32(acc_b + cc, rb);
+      tmem_ld_wait(rb);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        r[i] = __float_as_uint(fmaf(corr, __uint_as_float(rb[i]), __uint_as_float(r[i])));
+    }
+    if (!store) continue;
+    if (kF32) {
+      uint4* out = static_cast<uint4*>(row_ptr);
+#pragma unroll
+      for (int qv = 0; qv < 8; ++qv) {
+        const int col = cc + qv * 4;
+        if (col < d) {
+          uint4 v;
+          v.x = __float_as_uint(__uint_as_float(r[qv * 4 + 0]) * mult);
+          v.y = __float_as_uint(__uint_as_float(r[qv * 4 + 1]) * mult);
+          v.z = __float_as_uint(__uint_as_float(r[qv * 4 + 2]) * mult);
+          v.w = __float_as_uint(__uint_as_float(r[qv * 4 + 3]) * mult);
+          out[col / 4] = v;
+        }
+      }
+    } else {
+      uint4* out = static_cast<uint4*>(row_ptr);
+#pragma unroll
+      for (int qv = 0; qv < 4; ++qv) {
+        const int col = cc + qv * 8;
+        if (col < d) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(r[qv * 8 + 0]) * mult,
+                            __uint_as_float(r[qv * 8 + 1]) * mult);
+          v.y = pack_bf16x2(__uint_as_float(r[qv * 8 + 2]) * mult,
+                            __uint_as_float(r[qv * 8 + 3]) * mult);
+          v.z = pack_bf16x2(__uint_as_float(r[qv * 8 + 4]) * mult,
+                            __uint_as_float(r[qv * 8 + 5]) * mult);
+          v.w = pack_bf16x2(__uint_as_float(r[qv * 8 + 6]) * mult,
+                            __uint_as_float(r[qv * 8 + 7]) * mult);
+          out[col / 8] = v;
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+  const float lo = __uint_as_float(x << 16);
+  const float hi = __uint_as_float(x & 0xffff0000u);
+  return pack_f16x2(lo, hi);
+}
+
+template <int DP, bool kCausal, bool kDkDv, bool kF32Grad>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
+                  const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmC2,
+                  const BwdParams p) {
+  using Cfg = BwdCfg<DP>;
+  constexpr int kStages = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + Cfg::kBarOff);
+  float* dsum = reinterpret_cast<float*>(smem + Cfg::kDsumOff);
+  const volatile int* abort_flag = &bars->abort;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+
+  // ---- work item ----
+  const int N = p.N, H = p.H;
+  const int ntiles = (N + kRows - 1) / kRows;
+  const int nblocks = (N + kBlk - 1) / kBlk;
+  const int BH = p.B * H;
+  const int item = blockIdx.x;
+  // longest first: dK/dV tiles near the start see the most queries (causal),
+  // dQ tiles near the end see the most keys
+  const int tile = kDkDv ? (item / BH) : (ntiles - 1 - item / BH);
+  const int bh = item % BH, b = bh / H, h = bh % H;
+  const int row0 = tile * kRows;
+  int i0, i1;  // streamed blocks [i0, i1)
+  if (kDkDv) {
+    i0 = kCausal ? (row0 / kBlk) : 0;
+    i1 = nblocks;
+  } else {
+    i0 = 0;
+    i1 = kCausal ? min(nblocks, (row0 + kRows) / kBlk) : nblocks;
+  }
+  const int nb = i1 - i0;
+
+  // ---- setup ----
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->r_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->c_full[s], 1);
+      mbar_init(&bars->c_empty[s], 1);
+      mbar_init(&bars->vec_full[s], 32);
+      mbar_init(&bars->conv_full[s], 32);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&bars->s_full[g], 1);
+      mbar_init(&bars->p_full[g], 128);
+    }
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->dsum, 256);
+    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->probe, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  bool run = true;
+  if (p.probe_timeout) {
+    if (threadIdx.x == 0 && !mbar_wait(&bars->probe, 0, abort_flag, kProbeBudget))
+      raise_abort(bars, p.status);
+    __syncthreads();
+    run = false;
+  }
+
+  uint8_t* sR1 = smem + Cfg::kR1Off;
+  uint8_t* sR2 = smem + Cfg::kR2Off;
+  auto stage_c1 = [&](int s) { return smem + Cfg::kStageOff + s * Cfg::kStageBytes; };
+  auto stage_c2 = [&](int s) { return stage_c1(s) + Cfg::kBlkTile; };
+  auto stage_c1h = [&](int s) { return stage_c1(s) + 2 * Cfg::kBlkTile; };
+  auto stage_vec = [&](int s) {
+    return reinterpret_cast<float*>(stage_c1(s) + 3 * Cfg::kBlkTile);
+  };
+
+  if (run && warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmR1);
+      tma_prefetch_desc(&tmR2);
+      tma_prefetch_desc(&tmC1);
+      tma_prefetch_desc(&tmC2);
+      mbar_arrive_expect_tx(&bars->r_full, 2 * Cfg::kRowTile);
+      for (int c = 0; c < Cfg::kChunks; ++c) {
+        tma_load_4d(sR1 + c * Cfg::kRowChunk, &tmR1, &bars->r_full, c * 64, h, row0, b);
+        tma_load_4d(sR2 + c * Cfg::kRowChunk, &tmR2, &bars->r_full, c * 64, h, row0, b);
+      }
+      int issued = 0;
+      for (int t = 0; t < nb; ++t) {
+        const int s = t % kStages, round = t / kStages;
+        if (round > 0 &&
+            !mbar_wait(&bars->c_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
+          raise_abort(bars, p.status);
+          break;
+        }
+        const int r = (i0 + t) * kBlk;
+        mbar_arrive_expect_tx(&bars->c_full[s], 2 * Cfg::kBlkTile);
+        for (int c = 0; c < Cfg::kChunks; ++c) {
+          tma_load_4d(stage_c1(s) + c * Cfg::kBlkChunk, &tmC1, &bars->c_full[s], c * 64, h, r, b);
+          tma_load_4d(stage_c2(s) + c * Cfg::kBlkChunk, &tmC2, &bars->c_full[s], c * 64, h, r, b);
+        }
+        issued = t + 1;
+      }
+      for (int t = max(0, issued - kStages); t < issued; ++t)
+        mbar_wait(&bars->c_full[t % kStages], (t / kStages) & 1, nullptr, kDrainBudget);
+      mbar_wait(&bars->r_full, 0, nullptr, kDrainBudget);
+    }
+    __syncwarp();
+  } else if (run && warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t kIdescSP = idesc_bf16(kRows, kBlk, false, false);
+      constexpr uint32_t kIdescAccBf = idesc_bf16(kRows, DP, false, true);
+      constexpr uint32_t kIdescAccH = idesc_f16(kRows, DP, false, true);
+      const int nks = (p.d + 15) / 16;
+      const uint32_t r1a = smem_u32(sR1), r2a = smem_u32(sR2);
+      bool ok = mbar_wait(&bars->r_full, 0, abort_flag, kWaitBudget);
+
+      auto issue_sp = [&](int t) {
+        const int s = t % kStages, buf = t & 1;
+        const uint32_t c1a = smem_u32(stage_c1(s)), c2a = smem_u32(stage_c2(s));
+        for (int kk = 0; kk < nks; ++kk) {
+          const uint32_t ro = (kk >> 2) * Cfg::kRowChunk + (kk & 3) * 32;
+          const uint32_t co = (kk >> 2) * Cfg::kBlkChunk + (kk & 3) * 32;
+          mma_ss(tmem + Cfg::kTS + buf * kBlk, sdesc_sw128(r1a + ro, 16, 1024),
+                 sdesc_sw128(c1a + co, 16, 1024), kIdescSP, kk > 0);
+          mma_ss(tmem + Cfg::kTdP + buf * kBlk, sdesc_sw128(r2a + ro, 16, 1024),
+                 sdesc_sw128(c2a + co, 16, 1024), kIdescSP, kk > 0);
+        }
+        mma_commit(&bars->s_full[buf]);
+      };
+      auto issue_acc = [&](int t) {
+        const int s = t % kStages, buf = t & 1;
+        const uint32_t c1h = smem_u32(stage_c1h(s)), c2a = smem_u32(stage_c2(s));
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk) {
+          const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t pa = tmem + Cfg::kTS + buf * kBlk + kk * 8;    // P
+          const uint32_t da = tmem + Cfg::kTdP + buf * kBlk + kk * 8;   // dS
+          if (kDkDv)  // dV += P dO_i (bf16)
+            mma_ts(tmem + Cfg::kTAcc1, pa, sdesc_sw128(c2a + kk * 2048, Cfg::kBlkChunk, 1024),
+                   kIdescAccBf, acc);
+          else        // B += P K_j (fp16)
+            mma_ts(tmem + Cfg::kTAcc1, pa, sdesc_sw128(c1h + kk * 2048, Cfg::kBlkChunk, 1024),
+                   kIdescAccH, acc);
+          // dK += dS Q_i   or   dQ += dS K_j   (fp16)
+          mma_ts(tmem + Cfg::kTAcc2, da, sdesc_sw128(c1h + kk * 2048, Cfg::kBlkChunk, 1024),
+                 kIdescAccH, acc);
+        }
+        mma_commit(&bars->c_empty[s]);
+      };
+      auto ready_acc = [&](int t) {
+        return mbar_wait(&bars->p_full[t & 1], (t >> 1) & 1, abort_flag, kWaitBudget) &&
+               mbar_wait(&bars->conv_full[t % kStages], (t / kStages) & 1, abort_flag,
+                         kWaitBudget);
+      };
+
+      for (int t = 0; t < nb && ok; ++t) {
+        if (!mbar_wait(&bars->c_full[t % kStages], (t / kStages) & 1, abort_flag, kWaitBudget)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_sp(t);
+        if (t >= 1) {
+          if (!ready_acc(t - 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_acc(t - 1);
+        }
+      }
+      if (ok) {
+        if (ready_acc(nb - 1)) {
+          tc_fence_after();
+          issue_acc(nb - 1);
+          mma_commit(&bars->acc_full);
+        } else {
+          ok = false;
+        }
+      }
+      if (!ok) raise_abort(bars, p.status);
+      mma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, nullptr, kDrainBudget);
+    }
+    __syncwarp();
+  } else if (run && warp == 2) {
+    // ============ per-query L and D of each streamed block (dK/dV) ============
+    if (kDkDv) {
+      const float* lse = p.lse + static_cast<size_t>(bh) * N;
+      const float* Dv = p.D + static_cast<size_t>(bh) * N;
+      for (int t = 0; t < nb; ++t) {
+        const int s = t % kStages, round = t / kStages;
+        if (round > 0 &&
+            !warp_wait(&bars->c_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
+          if (lane == 0) raise_abort(bars, p.status);
+          break;
+        }
+        float* vec = stage_vec(s);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int c = u * 32 + lane;
+          const int q = (i0 + t) * kBlk + c;
+          float l2 = INFINITY, dd = 0.0f;   // padded or fully masked query: P = 0
+          if (q < N) {
+            const float L = lse[q];
+            if (L != -INFINITY) {
+              l2 = L * kLog2e;
+              dd = Dv[q];
+            }
+          }
+          vec[c] = l2;
+          vec[kBlk + c] = dd;
+        }
+        mbar_arrive(&bars->vec_full[s]);
+      }
+    }
+    __syncwarp();
+  } else if (run && warp == 3) {
+    // ============ fp16 copy of each streamed C1 tile (same swizzled layout) ============
+    constexpr int kVecs = Cfg::kBlkTile / 16;
+    for (int t = 0; t < nb; ++t) {
+      const int s = t % kStages;
+      if (!warp_wait(&bars->c_full[s], (t / kStages) & 1, abort_flag, kWaitBudget)) {
+        if (lane == 0) raise_abort(bars, p.status);
+        break;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(stage_c1(s));
+      uint4* dst = reinterpret_cast<uint4*>(stage_c1h(s));
+#pragma unroll 4
+      for (int i = lane; i < kVecs; i += 32) {
+        uint4 v = src[i];
+        v.x = bf16x2_to_f16x2(v.x);
+        v.y = bf16x2_to_f16x2(v.y);
+        v.z = bf16x2_to_f16x2(v.z);
+        v.w = bf16x2_to_f16x2(v.w);
+        dst[i] = v;
+      }
+      fence_proxy_async_smem();   // make the copy visible to the tensor cores
+      mbar_arrive(&bars->conv_full[s]);
+    }
+    __syncwarp();
+  } else if (run && warp >= 4) {
+    // ======================= element-wise warpgroups =======================
+    const int g = (warp - 4) / 4;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int grow = row0 + row;                    // query (dQ) or key (dK/dV)
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + Cfg::kTS + g * kBlk;
+    const uint32_t tdP = tmem + lane_base + Cfg::kTdP + g * kBlk;
+    const float c = p.scale_log2;
+    float l2_row = INFINITY, d_row = 0.0f;          // dQ kernel: this query's L, D~
+    bool live_row = false;
+    if (!kDkDv && grow < N) {
+      const float L = p.lse[static_cast<size_t>(bh) * N + grow];
+      if (L != -INFINITY) {
+        live_row = true;
+        l2_row = L * kLog2e;
+        d_row = p.D[static_cast<size_t>(bh) * N + grow];
+      }
+    }
+    float d_acc = 0.0f;                             // dQ kernel: sum_j P_ij dP_ij
+    bool ok = true;
+    for (int t = g; t < nb; t += 2) {
+      if (!warp_wait(&bars->s_full[g], (t >> 1) & 1, abort_flag, kWaitBudget)) {
+        ok = false;
+        break;
+      }
+      const int s = t % kStages;
+      if (kDkDv && !warp_wait(&bars->vec_full[s], (t / kStages) & 1, abort_flag, kWaitBudget)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int col0 = (i0 + t) * kBlk;             // first key (dQ) or query (dK/dV)
+      bool masked;
+      if (kDkDv) masked = kCausal && (col0 < row0 + kRows - 1);
+      else masked = (kCausal && (col0 + kBlk - 1 > row0)) || (col0 + kBlk > N);
+      const float* vec = kDkDv ? stage_vec(s) : nullptr;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tS + half * 32, sr);
+        tmem_ld32(tdP + half * 32, dr);
+        tmem_ld_wait(sr);
+        tmem_ld_wait(dr);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float pp[2], ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int cl = half * 32 + 2 * i + e;    // column within the block
+            const float sv = __uint_as_float(sr[2 * i + e]);
+            const float dpv = __uint_as_float(dr[2 * i + e]);
+            float l2, dd;
+            if (kDkDv) {
+              l2 = vec[cl];
+              dd = vec[kBlk + cl];
+            } else {
+              l2 = l2_row;
+              dd = d_row;
+            }
+            float pv = fast_exp2(fmaf(sv, c, -l2));
+            if (masked) {
+              const int other = col0 + cl;
+              const bool bad = kDkDv ? (other < grow)
+                                     : ((kCausal && other > grow) || other >= N);
+              if (bad) pv = 0.0f;
+            }
+            if (!kDkDv) d_acc = fmaf(pv, dpv, d_acc);
+            pp[e] = pv;
+            ds[e] = pv * (dpv - dd);
+          }
+          pk[i] = kDkDv ? pack_bf16x2(pp[0], pp[1]) : pack_f16x2(pp[0], pp[1]);
+          dk[i] = pack_f16x2(ds[0], ds[1]);
+        }
+        tmem_st16(tS + half * 16, pk);
+        tmem_st16(tdP + half * 16, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[g]);
+    }
+
+    // ---- epilogue: this warpgroup stores half of the accumulator columns ----
+    float corr = 0.0f;
+    if (!kDkDv && ok) {
+      // Combine the two warpgroups' partial sums of D_i = sum_j P_ij dP_ij.
+      dsum[g * kRows + row] = d_acc;
+      mbar_arrive(&bars->dsum);
+      if (!warp_wait(&bars->dsum, 0, abort_flag, kWaitBudget)) ok = false;
+      if (ok) {
+        const float d_exact = dsum[row] + dsum[kRows + row];
+        corr = d_row - d_exact;
+        if (g == 0 && live_row) p.D[static_cast<size_t>(bh) * N + grow] = d_exact;
+      }
+    }
+    if (ok && !warp_wait(&bars->acc_full, 0, abort_flag, kWaitBudget)) ok = false;
+    if (ok) {
+      tc_fence_after();
+      const bool store = grow < N;
+      const size_t roff = ((static_cast<size_t>(b) * N + (store ? grow : 0)) * H + h) *
+                          static_cast<size_t>(p.d);
+      const int half_cols = DP / 2;
+      const int cbeg = g * half_cols;
+      const uint32_t tbase = tmem + lane_base;
+      auto row_ptr = [&](void* base) -> void* {
+        return kF32Grad ? static_cast<void*>(static_cast<float*>(base) + roff)
+                        : static_cast<void*>(static_cast<__nv_bfloat16*>(base) + roff);
+      };
+      if (kDkDv) {
+        store_acc_cols<kF32Grad, false>(tbase + Cfg::kTAcc1, 0, 0.0f, cbeg, half_cols, 1.0f,
+                                        row_ptr(p.dv), p.d, store);
+        store_acc_cols<kF32Grad, false>(tbase + Cfg::kTAcc2, 0, 0.0f, cbeg, half_cols, p.scale,
+                                        row_ptr(p.dk), p.d, store);
+      } else {
+        store_acc_cols<kF32Grad, true>(tbase + Cfg::kTAcc2, tbase + Cfg::kTAcc1, corr, cbeg,
+                                       half_cols, p.scale, row_ptr(p.dq), p.d, store);
+      }
+    }
+    if (!ok) raise_abort(bars, p.status);
+    __syncwarp();
+  }
+
+  // ---- teardown ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int DP, bool kCausal, bool kDkDv, bool kF32>
+cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
+  using Cfg = BwdCfg<DP>;
+  CUtensorMap m[4];
+  // dQ:    rows are Q, dO (128-row boxes), blocks are K, V (64-row boxes).
+  // dK/dV: rows are K, V, blocks are Q, dO.
+  const void* r1 = kDkDv ? p.k : p.q;
+  const void* r2 = kDkDv ? p.v : p.dO;
+  const void* c1 = kDkDv ? p.q : p.k;
+  const void* c2 = kDkDv ? p.dO : p.v;
+  cudaError_t e = make_bhnd_tmap(&m[0], r1, p.B, p.N, p.H, p.d, kRows, 64);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&m[1], r2, p.B, p.N, p.H, p.d, kRows, 64);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&m[2], c1, p.B, p.N, p.H, p.d, kBlk, 64);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&m[3], c2, p.B, p.N, p.H, p.d, kBlk, 64);
+  if (e != cudaSuccess) return e;
+  auto kern = bwd_tc_kernel<DP, kCausal, kDkDv, kF32>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long items = static_cast<long long>((p.N + kRows - 1) / kRows) * p.B * p.H;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  BwdParams pc = p;
+  void* args[] = {&m[0], &m[1], &m[2], &m[3], &pc};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(static_cast<unsigned>(items)),
+                          dim3(kThreads), args, Cfg::kSmemBytes, st);
+}
+
+// dQ first: it refines D in the workspace, which the dK/dV kernel then reads.
+template <int DP, bool kCausal, bool kF32>
+cudaError_t launch_pair(const BwdParams& p, cudaStream_t st) {
+  cudaError_t e = launch_one<DP, kCausal, false, kF32>(p, st);
+  if (e != cudaSuccess) return e;
+  return launch_one<DP, kCausal, true, kF32>(p, st);
+}
+
+template <int DP>
+cudaError_t launch_dp(const BwdParams& p, cudaStream_t st, bool causal) {
+  if (causal) return p.grad_f32 ? launch_pair<DP, true, true>(p, st)
+                                : launch_pair<DP, true, false>(p, st);
+  return p.grad_f32 ? launch_pair<DP, false, true>(p, st) : launch_pair<DP, false, false>(p, st);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc_bf16(const BwdParams& p, cudaStream_t s, bool causal) {
+  if (p.d <= 64) return launch_dp<64>(p, s, causal);
+  if (p.d <= 128) return launch_dp<128>(p, s, causal);
   return cudaErrorNotSupported;
 }
 

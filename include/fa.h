@@ -93,9 +93,15 @@ size_t fa_bwd_workspace_size(int B, int H, int N);
  *   dq, dk, dv     out : [B, N, H, d], element type `grad_dtype`
  *   grad_dtype         : `dtype`, or FA_DTYPE_F32 for float32 gradients
  *   workspace          : device scratch of >= fa_bwd_workspace_size(B,H,N)
- *                        bytes, 256-byte aligned; contents on entry ignored
+ *                        bytes, 256-byte aligned; contents on entry ignored;
+ *                        on return it holds D as float32 [B, H, N]
  *   other arguments as in fa_fwd.
  * Rows whose lse is -inf (no visible key) contribute nothing.
+ *
+ * bf16 path: D is first taken from the bf16 O as above, then refined in the
+ * dQ kernel to the fp32 sum_j P_ij dP_ij (the same quantity without O's
+ * storage rounding), and dQ is corrected accordingly; dS is staged for the
+ * tensor cores in fp16, so |Q|, |K| and |dS| must stay below 65504.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  const float* lse, const void* dO,

@@ -1,0 +1,172 @@
+"""Backward parity on the GPU: dQ, dK, dV (and the D pre-pass) through the C ABI
+against the float64 oracle's analytic gradients on the same seeded inputs."""
+
+import os
+
+import numpy as np
+import pytest
+
+from exact_attention_fwd_gb300.configs import BROWSER_SHAPE, WORKLOADS
+from exact_attention_fwd_gb300.inputs import torch_to_f64
+from tests.gpu_util import TOL, default_scale, make, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd_bwd(inp, causal, scale=None, grad_f32=False):
+    import torch
+    from exact_attention_fwd_gb300 import api
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (inp.torch(t, dev) for t in ("q", "k", "v", "do"))
+    o, lse = api.forward(q, k, v, scale=scale, causal=causal)
+    ws = api.workspace(inp.B, inp.H, inp.N, dev)
+    gdt = torch.float32 if grad_f32 else None
+    dq, dk, dv = api.backward(q, k, v, o, lse, do, scale=scale, causal=causal, grad_dtype=gdt,
+                              ws=ws)
+    st = api.sync_status()
+    assert st == 0, f"device status {st}"
+    return dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv, ws=ws)
+
+
+def compare_bwd(inp, out, causal, scale, tol, heads=None):
+    from oracle import attention as A
+    from oracle import checker
+    heads = heads or [(b, h) for b in range(inp.B) for h in range(inp.H)]
+    got = {n: torch_to_f64(out[n]) for n in ("dq", "dk", "dv")}
+    worst = {n: 0.0 for n in got}
+    for b, h in heads:
+        g = A.backward_head(inp.head_f64("q", b, h), inp.head_f64("k", b, h),
+                            inp.head_f64("v", b, h), inp.head_f64("do", b, h), scale, causal)
+        for n in got:
+            ok, err, nbad = checker.check(got[n][b, :, h, :], g[n], tol)
+            assert ok, f"{n} head {(b, h)}: max err {err:.3e}, {nbad} mismatches"
+            worst[n] = max(worst[n], err)
+    return worst
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("sub", range(5))
+def test_causal_sweep_backward(dtype, sub):
+    """Workload 1: the pages' causal parity shapes, fp32 and bf16."""
+    require_gpu()
+    w = WORKLOADS[1]
+    s = w.shapes[sub]
+    inp = make(s.B, s.H, s.N, s.d, dtype, w.seed(sub))
+    out = run_fwd_bwd(inp, causal=True)
+    compare_bwd(inp, out, True, w.scale(s), TOL[dtype]["grad"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_browser_shape_backward(dtype, causal):
+    require_gpu()
+    s = BROWSER_SHAPE
+    inp = make(s.B, s.H, s.N, s.d, dtype, 5100 + int(causal))
+    out = run_fwd_bwd(inp, causal=causal)
+    compare_bwd(inp, out, causal, default_scale(s.d), TOL[dtype]["grad"])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 2, 63, 64, 65, 127, 128, 129, 200, 256, 300, 449])
+def test_ragged_n_backward_bf16(causal, N):
+    require_gpu()
+    inp = make(1, 2, N, 64, "bf16", 9000 + N)
+    out = run_fwd_bwd(inp, causal=causal)
+    compare_bwd(inp, out, causal, default_scale(64), TOL["bf16"]["grad"])
+
+
+@pytest.mark.parametrize("d", [8, 16, 32, 40, 64, 96, 128])
+def test_head_dims_backward_bf16(d):
+    require_gpu()
+    inp = make(2, 2, 200, d, "bf16", 9500 + d)
+    for causal in (False, True):
+        out = run_fwd_bwd(inp, causal=causal)
+        compare_bwd(inp, out, causal, default_scale(d), TOL["bf16"]["grad"])
+
+
+@pytest.mark.parametrize("d", [8, 32, 64, 128])
+def test_head_dims_backward_f32(d):
+    require_gpu()
+    inp = make(1, 2, 90, d, "f32", 9600 + d)
+    for causal in (False, True):
+        out = run_fwd_bwd(inp, causal=causal)
+        compare_bwd(inp, out, causal, default_scale(d), TOL["f32"]["grad"])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_gradients_of_bf16_inputs(causal):
+    """grad_dtype = F32: same accumulation, float32 stores; the tolerance is the
+    bf16 one (the inputs and P are bf16) but there is no output rounding."""
+    require_gpu()
+    inp = make(2, 2, 333, 64, "bf16", 9700, sigma={"q": 4.0, "k": 4.0})
+    out = run_fwd_bwd(inp, causal=causal, grad_f32=True)
+    worst = compare_bwd(inp, out, causal, default_scale(64), TOL["bf16"]["grad"])
+    assert all(e < TOL["bf16"]["grad"] for e in worst.values())
+
+
+def test_large_scores_backward_bf16():
+    require_gpu()
+    inp = make(1, 2, 500, 64, "bf16", 9800, sigma={"q": 4.0, "k": 4.0})
+    for causal in (False, True):
+        out = run_fwd_bwd(inp, causal=causal, grad_f32=True)
+        compare_bwd(inp, out, causal, default_scale(64), TOL["bf16"]["grad"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_workspace_d_matches_oracle(dtype):
+    """After fa_bwd the workspace holds D = rowsum(dO * O), [B, H, N]: from the
+    fp32 O for fp32 inputs; refined to sum_j P_ij dP_ij for bf16 inputs."""
+    torch = require_gpu()
+    from oracle import attention as A
+    inp = make(2, 3, 257, 64, dtype, 9900, sigma={"q": 4.0, "k": 4.0})
+    out = run_fwd_bwd(inp, causal=True)
+    n = inp.B * inp.H * inp.N
+    D = out["ws"][: 4 * n].view(torch.float32).cpu().double().numpy()
+    D = D.reshape(inp.B, inp.H, inp.N)
+    for b in range(inp.B):
+        for h in range(inp.H):
+            g = A.backward_head(inp.head_f64("q", b, h), inp.head_f64("k", b, h),
+                                inp.head_f64("v", b, h), inp.head_f64("do", b, h),
+                                default_scale(64), True)
+            # fp32 sums of d products of magnitude up to |D|: relative bound
+            assert np.all(np.abs(D[b, h] - g["D"]) <= 1e-4 * np.maximum(1.0, np.abs(g["D"])))
+
+
+def test_gradient_invariants_on_gpu_output():
+    """Sum over keys of dK is zero and sum over keys of dV equals sum over
+    queries of dO (both hold for the exact gradient at any size)."""
+    require_gpu()
+    inp = make(1, 2, 640, 64, "bf16", 9910)
+    out = run_fwd_bwd(inp, causal=True, grad_f32=True)
+    dk, dv = torch_to_f64(out["dk"]), torch_to_f64(out["dv"])
+    do64 = inp.f64("do")
+    assert np.max(np.abs(dk.sum(axis=1))) < 0.5
+    assert np.max(np.abs(dv.sum(axis=1) - do64.sum(axis=1))) < 0.5
+
+
+def test_backward_repeat_is_bitwise_deterministic():
+    torch = require_gpu()
+    inp = make(1, 2, 390, 128, "bf16", 9920)
+    a = run_fwd_bwd(inp, causal=True)
+    b = run_fwd_bwd(inp, causal=True)
+    for n in ("dq", "dk", "dv"):
+        assert torch.equal(a[n], b[n]), n
+
+
+def test_backward_bounded_wait_self_test():
+    torch = require_gpu()
+    from exact_attention_fwd_gb300 import _lib, api
+    inp = make(1, 2, 256, 64, "bf16", 9930)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (inp.torch(t, dev) for t in ("q", "k", "v", "do"))
+    o, lse = api.forward(q, k, v, causal=True)
+    assert api.sync_status() == 0
+    os.environ["FA_SELFTEST_WAIT_TIMEOUT"] = "1"
+    try:
+        api.backward(q, k, v, o, lse, do, causal=True)
+        st = api.sync_status()
+    finally:
+        del os.environ["FA_SELFTEST_WAIT_TIMEOUT"]
+    assert st == _lib.FA_ERR_TIMEOUT
+    dq, dk, dv = api.backward(q, k, v, o, lse, do, causal=True)
+    assert api.sync_status() == 0
