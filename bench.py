@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark: fused exact attention forward + backward on GB300, TFLOP/s.
+
+One step = the whole hot path over one batch of the GPT-2-medium-shaped
+workload (B=64, H=16, N=1024, d=64, causal, bf16 in / fp32 accumulate):
+fa_fwd, then the backward's three kernels (D pre-pass, dQ, dK/dV).  FLOPs are
+credited as 4 B H N^2 d for the forward (halved when causal) and 2.5x that for
+the backward.  Inputs are seeded normals (no dataset), 134 MB per tensor, so
+every step's working set (~1 GB) is far larger than the 126 MB L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  --impl reference times the float64 CPU oracle on a
+bounded sample (one head per step) of the same workload.  Under torchrun each
+rank runs its own full batch (weak scaling, no data-path collective) and rank
+0 prints the aggregate.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+WORKLOAD = dict(name="gpt2_medium_attention", B=64, H=16, N=1024, d=64, causal=True,
+                dtype="bf16", seed=2000)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# Source file of each kernel: a traffic figure measured by ncu is reported only
+# while the source it was measured on is unchanged.
+KERNELS = {
+    "fwd_tc_kernel": "exact_attention_fwd_gb300/csrc/tc_fwd.cu",
+    "dot_do_o_kernel": "exact_attention_fwd_gb300/csrc/bwd_dot.cu",
+    "bwd_dq": "exact_attention_fwd_gb300/csrc/tc_bwd.cu",
+    "bwd_dkdv": "exact_attention_fwd_gb300/csrc/tc_bwd.cu",
+}
+
+
+# ----------------------------------------------------------------------------
+# host-side helpers (also used by the CPU tests)
+# ----------------------------------------------------------------------------
+
+def flops_step(B, H, N, d, causal):
+    fwd = 4.0 * B * H * N * N * d * (0.5 if causal else 1.0)
+    return fwd, 2.5 * fwd
+
+
+def kernel_work(B, H, N, d, causal, elt=2):
+    """Algorithmic work per launch of each kernel of a step.
+
+    fwd_tc_kernel: S = Q K^T and O = P V, 2 matmuls of 2 N^2 d per head.
+    dot_do_o_kernel: bytes of O and dO read plus D written.
+    bwd_dq: S, dP and dQ (3 matmuls); bwd_dkdv: S, dP, dV, dK (4 matmuls);
+    the backward recomputes S and dP in both kernels so that no float atomics
+    are needed.  Causal halves every matmul count.
+    """
+    half = 0.5 if causal else 1.0
+    mm = 2.0 * B * H * N * N * d * half
+    return {
+        "fwd_tc_kernel": ("tensor", 2 * mm),
+        "dot_do_o_kernel": ("hbm", 2.0 * B * H * N * d * elt + 4.0 * B * H * N),
+        "bwd_dq": ("tensor", 3 * mm),
+        "bwd_dkdv": ("tensor", 4 * mm),
+    }
+
+
+def aggregate(units_per_rank, seconds_per_rank):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    return sum(units_per_rank) / max(seconds_per_rank)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(relpath):
+    with open(os.path.join(ROOT, relpath), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(kernel)
+    if not e or e.get("source_sha") != source_sha(KERNELS[kernel]):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def parse_clocks(lines):
+    """Summary of nvidia-smi CSV samples: median SM clock, max, reasons seen."""
+    sm, smax, reasons = [], [], set()
+    names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+             "sw_power_cap"]
+    for ln in lines:
+        parts = [x.strip() for x in ln.split(",")]
+        if len(parts) < 9 or not parts[1].replace(".", "").isdigit():
+            continue
+        sm.append(float(parts[1]))
+        smax.append(float(parts[2]))
+        for name, val in zip(names[1:], parts[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = out.splitlines()
+        return False
+
+    def summary(self):
+        return parse_clocks(getattr(self, "lines", []))
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def oracle_head_step(inp, b, h, scale, causal):
+    from oracle import attention as A
+    q, k, v, do = (inp.head_f64(t, b, h) for t in ("q", "k", "v", "do"))
+    A.forward_head(q, k, v, scale, causal)
+    A.backward_head(q, k, v, do, scale, causal)
+
+
+def cpu_oracle_rate(inp, scale, causal, budget_s, max_heads=None):
+    """Time the oracle's fwd+bwd on heads of `inp` until `budget_s` seconds of
+    work; returns (TFLOP/s credited, heads, seconds)."""
+    heads = [(b, h) for b in range(inp.B) for h in range(inp.H)]
+    fwd, bwd = flops_step(1, 1, inp.N, inp.d, causal)
+    t0 = time.perf_counter()
+    n = 0
+    for b, h in heads:
+        oracle_head_step(inp, b, h, scale, causal)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s or (max_heads and n >= max_heads):
+            break
+    dt = time.perf_counter() - t0
+    return n * (fwd + bwd) / dt / 1e12, n, dt
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def init_dist(world, use_cuda):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("nccl" if use_cuda else "gloo")
+    return dist
+
+
+def max_over_ranks(x, dist, device=None):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+
+    from exact_attention_fwd_gb300 import api, build
+    from exact_attention_fwd_gb300.inputs import Inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = init_dist(world, True)
+    W = WORKLOAD
+    B, H, N, d, causal = W["B"], W["H"], W["N"], W["d"], W["causal"]
+    scale = 1.0 / math.sqrt(d)
+    inp = Inputs(B, H, N, d, "bf16", W["seed"] + rank)
+    host = {t: torch.from_numpy(inp.storage[t].view("int16")).view(torch.bfloat16).pin_memory()
+            for t in ("q", "k", "v", "do")}
+    q, k, v, do = (host[t].to(dev) for t in ("q", "k", "v", "do"))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    ws = api.workspace(B, H, N, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        api.forward(q, k, v, scale=scale, causal=causal, out=o, lse=lse)
+        for ph in range(3):
+            if evs:
+                evs[ph + 1].record(stream)
+            api.backward(q, k, v, o, lse, do, scale=scale, causal=causal, ws=ws, dq=dq, dk=dk,
+                         dv=dv, phase=ph)
+        if evs:
+            evs[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if api.sync_status() != 0:
+        raise SystemExit("device status word set during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for i in range(K):
+            step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    status = api.sync_status()
+    if status != 0:
+        raise SystemExit(f"device status word {status} after the timed region")
+    t_ms = start.elapsed_time(end)
+    t_ms_max = max_over_ranks(t_ms, dist, dev)
+    names = ["fwd_tc_kernel", "dot_do_o_kernel", "bwd_dq", "bwd_dkdv"]
+    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+           for j, n in enumerate(names)}
+
+    fwd_fl, bwd_fl = flops_step(B, H, N, d, causal)
+    value = aggregate([K * (fwd_fl + bwd_fl)] * world, [t_ms_max / 1e3] * world) / 1e12
+
+    peaks, peak_src = load_peaks()
+    work = kernel_work(B, H, N, d, causal)
+    dom = max(names, key=lambda n: per[n])
+    bound, amount = work[dom]
+    if bound == "tensor":
+        peak, unit_r = peaks["bf16_tflops"], "TFLOP/s"
+        achieved = amount / (per[dom] / 1e3) / 1e12
+    else:
+        peak, unit_r = peaks["hbm_gbs"], "GB/s"
+        achieved = amount / (per[dom] / 1e3) / 1e9
+    kernels = {}
+    for n in names:
+        bnd, amt = work[n]
+        rate = amt / (per[n] / 1e3) / (1e12 if bnd == "tensor" else 1e9)
+        pk = peaks["bf16_tflops"] if bnd == "tensor" else peaks["hbm_gbs"]
+        kernels[n] = {"ms": round(per[n], 4), "share": round(per[n] / sum(per.values()), 4),
+                      "bound": bnd, "achieved": round(rate, 1), "frac": round(rate / pk, 4)}
+
+    # end to end through the public API: pinned host inputs in, results out
+    e2e = None
+    if not args.no_e2e:
+        Ke = max(3, min(K, args.e2e_steps))
+        out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+
+        def e2e_step():
+            qd, kd, vd, dod = (host[t].to(dev, non_blocking=True) for t in ("q", "k", "v", "do"))
+            oo, ll = api.forward(qd, kd, vd, scale=scale, causal=causal)
+            gq, gk, gv = api.backward(qd, kd, vd, oo, ll, dod, scale=scale, causal=causal, ws=ws)
+            for n, t in (("o", oo), ("lse", ll), ("dq", gq), ("dk", gk), ("dv", gv)):
+                out_host[n].copy_(t, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize(dev)
+        te = max_over_ranks(s2.elapsed_time(e2), dist, dev)
+        h2d = sum(host[t].numel() * host[t].element_size() for t in ("q", "k", "v", "do"))
+        d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+        e2e = {"value": round(world * Ke * (fwd_fl + bwd_fl) / (te / 1e3) / 1e12, 2),
+               "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(te / Ke, 3), "steps": Ke}
+        if api.sync_status() != 0:
+            raise SystemExit("device status word set during the end-to-end run")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, nh, secs = cpu_oracle_rate(inp, scale, causal, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{nh} of {B * H} heads of the same workload, float64 numpy fwd+bwd "
+                         f"({secs:.1f} s), FLOPs credited as for the GPU"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(t_ms_max / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": W["name"], "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                   "io": "bf16 in/out, fp32 accumulate", "global_batch": B * world,
+                   "seq_len": N, "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": "inputs larger than L2 (134 MB per tensor, ~1 GB per step)"},
+        "passes": {
+            "fwd": {"ms": round(per["fwd_tc_kernel"], 4),
+                    "tflops": round(fwd_fl / (per["fwd_tc_kernel"] / 1e3) / 1e12, 1),
+                    "pct_peak": round(100 * fwd_fl / (per["fwd_tc_kernel"] / 1e3) / 1e12
+                                      / peaks["bf16_tflops"], 2)},
+            "bwd": {"ms": round(sum(per[n] for n in names[1:]), 4),
+                    "tflops": round(bwd_fl / (sum(per[n] for n in names[1:]) / 1e3) / 1e12, 1),
+                    "pct_peak": round(100 * bwd_fl / (sum(per[n] for n in names[1:]) / 1e3)
+                                      / 1e12 / peaks["bf16_tflops"], 2)},
+            "step_pct_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
+        },
+        "kernels": kernels,
+        "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": unit_r, "frac": round(achieved / peak, 4),
+                     "traffic": traffic_for(dom), "peak_source": peak_src + " (burst)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 4 * K,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The float64 CPU oracle as the reference arm: each step is one head of
+    the same workload (fwd+bwd), rank 0 only."""
+    if rank != 0:
+        return
+    from exact_attention_fwd_gb300.inputs import Inputs
+    W = WORKLOAD
+    B, H, N, d, causal = W["B"], W["H"], W["N"], W["d"], W["causal"]
+    scale = 1.0 / math.sqrt(d)
+    # only the heads the steps use are needed: draw a batch of 1 with the
+    # workload's per-head shape (same distribution, same recipe)
+    inp = Inputs(1, H, N, d, "bf16", W["seed"])
+    heads = [(0, h) for h in range(H)]
+    for i in range(args.warmup):
+        oracle_head_step(inp, *heads[i % H], scale, causal)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_head_step(inp, *heads[i % H], scale, causal)
+    dt = time.perf_counter() - t0
+    fwd, bwd = flops_step(1, 1, N, d, causal)
+    value = args.steps * (fwd + bwd) / dt / 1e12
+    cores = blas_threads()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": W["name"], "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                   "io": "bf16-rounded inputs, float64 arithmetic", "global_batch": B,
+                   "seq_len": N, "parallelism": "CPU oracle, one head per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "one (b, h) head of the workload per step, float64 numpy "
+                                   "fwd+bwd"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, local_rank, world = dist_env()
+    if world != args.gpus and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, local_rank, world)
+
+
+if __name__ == "__main__":
+    main()

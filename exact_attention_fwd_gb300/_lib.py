@@ -14,7 +14,8 @@ LIB_PATH = os.path.join(PKG, "libfa.so")
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F16 = range(3)
 
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_sync_status", "fa_status_string")
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_phase", "fa_bwd_workspace_size", "fa_sync_status",
+           "fa_status_string")
 
 _lib = None
 
@@ -39,6 +40,8 @@ def load():
     lib.fa_fwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp, sz, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_phase.argtypes = [i] + lib.fa_bwd.argtypes
+    lib.fa_bwd_phase.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i]
     lib.fa_bwd_workspace_size.restype = sz
     lib.fa_sync_status.argtypes = [vp]
@@ -63,6 +66,13 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, dtype, gr
            workspace, workspace_bytes, stream):
     return load().fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, float(scale), int(causal),
                          int(dtype), int(grad_dtype), workspace, workspace_bytes, stream)
+
+
+def fa_bwd_phase(phase, q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, dtype,
+                 grad_dtype, workspace, workspace_bytes, stream):
+    return load().fa_bwd_phase(int(phase), q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d,
+                               float(scale), int(causal), int(dtype), int(grad_dtype), workspace,
+                               workspace_bytes, stream)
 
 
 def fa_bwd_workspace_size(B, H, N):

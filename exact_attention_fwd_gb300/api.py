@@ -57,7 +57,7 @@ def workspace(B, H, N, device):
 
 
 def backward(q, k, v, o, lse, do, scale=None, causal=False, grad_dtype=None, ws=None,
-             dq=None, dk=None, dv=None, stream=None):
+             dq=None, dk=None, dv=None, stream=None, phase=None):
     """dQ, dK, dV of attention given the forward's O and LSE and the incoming dO."""
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _check(t, name, q.dtype)
@@ -72,12 +72,16 @@ def backward(q, k, v, o, lse, do, scale=None, causal=False, grad_dtype=None, ws=
     dv = torch.empty(q.shape, dtype=gdt, device=q.device) if dv is None else dv
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check(t, name, gdt)
-    st = _lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                     do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale,
-                     causal, _DTYPES[q.dtype], _DTYPES[gdt], ws.data_ptr(), ws.numel(),
-                     _stream_handle(stream))
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale,
+            causal, _DTYPES[q.dtype], _DTYPES[gdt], ws.data_ptr(), ws.numel(),
+            _stream_handle(stream))
+    if phase is None:
+        st = _lib.fa_bwd(*args)
+    else:
+        st = _lib.fa_bwd_phase(phase, *args)
     if st != _lib.FA_OK:
-        raise _lib.FaError(st, "fa_bwd")
+        raise _lib.FaError(st, "fa_bwd" if phase is None else f"fa_bwd_phase({phase})")
     return dq, dk, dv
 
 

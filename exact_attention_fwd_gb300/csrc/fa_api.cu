@@ -121,10 +121,15 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-                 float scale, int causal, fa_dtype dtype, fa_dtype grad_dtype, void* workspace,
-                 size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates fa_bwd's arguments and fills the launch parameters.
+fa_status prepare_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                      float scale, fa_dtype dtype, fa_dtype grad_dtype, void* workspace,
+                      size_t workspace_bytes, fa::BwdParams* out) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
     return FA_ERR_INVALID_ARG;
   if (dtype == FA_DTYPE_F16 || grad_dtype == FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
@@ -142,10 +147,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   const size_t l_bytes = static_cast<size_t>(B) * H * N * sizeof(float);
   const void* outs[] = {dq, dk, dv};
   const void* ins[] = {q, k, v, o, dO};
-  for (const void* out : outs) {
+  for (const void* outp : outs) {
     for (const void* in : ins)
-      if (overlaps(out, g_bytes, in, in_bytes)) return FA_ERR_INVALID_ARG;
-    if (overlaps(out, g_bytes, lse, l_bytes) || overlaps(out, g_bytes, workspace, workspace_bytes))
+      if (overlaps(outp, g_bytes, in, in_bytes)) return FA_ERR_INVALID_ARG;
+    if (overlaps(outp, g_bytes, lse, l_bytes) || overlaps(outp, g_bytes, workspace, workspace_bytes))
       return FA_ERR_INVALID_ARG;
   }
   if (overlaps(dq, g_bytes, dk, g_bytes) || overlaps(dq, g_bytes, dv, g_bytes) ||
@@ -159,7 +164,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   int* status = status_word(&err);
   if (status == nullptr) return err;
 
-  fa::BwdParams p{};
+  fa::BwdParams& p = *out;
+  p = fa::BwdParams{};
   p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.dO = dO;
   p.dq = dq; p.dk = dk; p.dv = dv;
   p.D = static_cast<float*>(workspace);
@@ -169,13 +175,53 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.grad_f32 = (grad_dtype == FA_DTYPE_F32) ? 1 : 0;
   p.status = status;
   p.probe_timeout = probe_timeout_requested() ? 1 : 0;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = fa::launch_bwd_dot(p, dtype == FA_DTYPE_BF16, s);
-  if (e == cudaSuccess)
-    e = (dtype == FA_DTYPE_F32) ? fa::launch_bwd_simt_f32(p, s, causal != 0)
-                                : fa::launch_bwd_tc_bf16(p, s, causal != 0);
+  return FA_OK;
+}
+
+fa_status run_bwd_phase(const fa::BwdParams& p, int phase, fa_dtype dtype, bool causal,
+                        cudaStream_t s) {
+  cudaError_t e;
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  if (phase == 0) {
+    e = fa::launch_bwd_dot(p, bf16, s);
+  } else if (!bf16) {
+    e = fa::launch_bwd_simt_f32(p, s, causal, phase);
+  } else {
+    e = fa::launch_bwd_tc_bf16(p, s, causal, phase);
+  }
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, fa_dtype grad_dtype, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  fa::BwdParams p;
+  fa_status st = prepare_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, dtype,
+                             grad_dtype, workspace, workspace_bytes, &p);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int phase = 0; phase < 3 && st == FA_OK; ++phase)
+    st = run_bwd_phase(p, phase, dtype, causal != 0, s);
+  return st;
+}
+
+fa_status fa_bwd_phase(int phase, const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                       int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                       fa_dtype grad_dtype, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  if (phase < 0 || phase > 2) return FA_ERR_INVALID_ARG;
+  fa::BwdParams p;
+  fa_status st = prepare_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, dtype,
+                             grad_dtype, workspace, workspace_bytes, &p);
+  if (st != FA_OK) return st;
+  return run_bwd_phase(p, phase, dtype, causal != 0, static_cast<cudaStream_t>(stream));
 }
 
 fa_status fa_sync_status(void* stream) {

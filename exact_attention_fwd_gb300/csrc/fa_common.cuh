@@ -56,11 +56,12 @@ struct BwdParams {
 
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_fwd_simt_f32(const FwdParams& p, cudaStream_t s, bool causal);
-cudaError_t launch_bwd_simt_f32(const BwdParams& p, cudaStream_t s, bool causal);
+cudaError_t launch_bwd_simt_f32(const BwdParams& p, cudaStream_t s, bool causal, int phase);
 cudaError_t launch_bwd_dot(const BwdParams& p, bool bf16, cudaStream_t s);
 // bf16 tensor-core path; returns cudaErrorNotSupported for shapes it does not
 // take.  Tensor maps are built inside from the raw pointers.
 cudaError_t launch_fwd_tc_bf16(const FwdParams& p, cudaStream_t s, bool causal);
-cudaError_t launch_bwd_tc_bf16(const BwdParams& p, cudaStream_t s, bool causal);
+// phase 1: dQ kernel (also refines D in the workspace); phase 2: dK/dV kernel.
+cudaError_t launch_bwd_tc_bf16(const BwdParams& p, cudaStream_t s, bool causal, int phase);
 
 }  // namespace fa

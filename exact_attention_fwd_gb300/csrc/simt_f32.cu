@@ -316,12 +316,15 @@ cudaError_t launch_fwd_simt_f32(const FwdParams& p, cudaStream_t s, bool causal)
                 : launch(fwd_simt_kernel<false>, grid, smem, s, &p);
 }
 
-cudaError_t launch_bwd_simt_f32(const BwdParams& p, cudaStream_t s, bool causal) {
-  const dim3 gk((p.N + kBC - 1) / kBC, p.B * p.H);
-  const size_t smem_k = sizeof(float) * (2 * kBC * p.d + 2 * kBR * (p.d + 1) + 2 * kBR);
-  cudaError_t e = causal ? launch(bwd_dkdv_simt_kernel<true>, gk, smem_k, s, &p)
-                         : launch(bwd_dkdv_simt_kernel<false>, gk, smem_k, s, &p);
-  if (e != cudaSuccess) return e;
+// phase 1: dQ kernel; phase 2: dK/dV kernel (either order works for fp32).
+cudaError_t launch_bwd_simt_f32(const BwdParams& p, cudaStream_t s, bool causal, int phase) {
+  if (phase == 2) {
+    const dim3 gk((p.N + kBC - 1) / kBC, p.B * p.H);
+    const size_t smem_k = sizeof(float) * (2 * kBC * p.d + 2 * kBR * (p.d + 1) + 2 * kBR);
+    return causal ? launch(bwd_dkdv_simt_kernel<true>, gk, smem_k, s, &p)
+                  : launch(bwd_dkdv_simt_kernel<false>, gk, smem_k, s, &p);
+  }
+  if (phase != 1) return cudaErrorInvalidValue;
   const dim3 gq((p.N + kBR - 1) / kBR, p.B * p.H);
   const size_t smem_q = sizeof(float) * (2 * kBR * p.d + 2 * kBC * (p.d + 1));
   return causal ? launch(bwd_dq_simt_kernel<true>, gq, smem_q, s, &p)

@@ -589,26 +589,28 @@ cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
                           dim3(kThreads), args, Cfg::kSmemBytes, st);
 }
 
-// dQ first: it refines D in the workspace, which the dK/dV kernel then reads.
+// Phase 1 is the dQ kernel: it refines D in the workspace, which the dK/dV
+// kernel (phase 2) then reads, so the phases run in that order.
 template <int DP, bool kCausal, bool kF32>
-cudaError_t launch_pair(const BwdParams& p, cudaStream_t st) {
-  cudaError_t e = launch_one<DP, kCausal, false, kF32>(p, st);
-  if (e != cudaSuccess) return e;
-  return launch_one<DP, kCausal, true, kF32>(p, st);
+cudaError_t launch_phase(const BwdParams& p, cudaStream_t st, int phase) {
+  return phase == 1 ? launch_one<DP, kCausal, false, kF32>(p, st)
+                    : launch_one<DP, kCausal, true, kF32>(p, st);
 }
 
 template <int DP>
-cudaError_t launch_dp(const BwdParams& p, cudaStream_t st, bool causal) {
-  if (causal) return p.grad_f32 ? launch_pair<DP, true, true>(p, st)
-                                : launch_pair<DP, true, false>(p, st);
-  return p.grad_f32 ? launch_pair<DP, false, true>(p, st) : launch_pair<DP, false, false>(p, st);
+cudaError_t launch_dp(const BwdParams& p, cudaStream_t st, bool causal, int phase) {
+  if (causal) return p.grad_f32 ? launch_phase<DP, true, true>(p, st, phase)
+                                : launch_phase<DP, true, false>(p, st, phase);
+  return p.grad_f32 ? launch_phase<DP, false, true>(p, st, phase)
+                    : launch_phase<DP, false, false>(p, st, phase);
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_tc_bf16(const BwdParams& p, cudaStream_t s, bool causal) {
-  if (p.d <= 64) return launch_dp<64>(p, s, causal);
-  if (p.d <= 128) return launch_dp<128>(p, s, causal);
+cudaError_t launch_bwd_tc_bf16(const BwdParams& p, cudaStream_t s, bool causal, int phase) {
+  if (phase != 1 && phase != 2) return cudaErrorInvalidValue;
+  if (p.d <= 64) return launch_dp<64>(p, s, causal, phase);
+  if (p.d <= 128) return launch_dp<128>(p, s, causal, phase);
   return cudaErrorNotSupported;
 }
 

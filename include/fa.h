@@ -111,6 +111,26 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_bwd_phase — one step of fa_bwd, for callers that schedule or time the
+ * backward's kernels separately.  fa_bwd is exactly phases 0, 1, 2 in order
+ * on one stream, and the phases must be run in that order:
+ *   0: the D pre-pass, D = rowsum(dO * O) into the workspace
+ *      ("Flash Attention 2 — backward pass notes", option 1 of "Why the WGSL
+ *      kernel isn't shipped this turn");
+ *   1: the kernel that owns Q tiles and writes dQ (bf16 path: also refines D
+ *      in the workspace);
+ *   2: the kernel that owns K tiles and writes dK and dV (option 3).
+ * Arguments, validation and errors as fa_bwd; phase outside [0, 2] returns
+ * FA_ERR_INVALID_ARG.
+ */
+fa_status fa_bwd_phase(int phase, const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dO,
+                       void* dq, void* dk, void* dv,
+                       int B, int H, int N, int d, float scale, int causal,
+                       fa_dtype dtype, fa_dtype grad_dtype,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fa_sync_status — synchronises `stream`, then returns and clears the device
  * status word of the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel's
  * bounded wait ran out since the last call (its outputs are then undefined),

@@ -83,3 +83,15 @@ def test_bwd_rejects_invalid_arguments(lib, kw, want):
              stream=None)
     a.update(kw)
     assert _lib.fa_bwd(**a) == want
+
+
+def test_bwd_phase_rejects_bad_phase(lib):
+    from exact_attention_fwd_gb300 import _lib
+    a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, dO=6 * FAKE,
+             dq=8 * FAKE, dk=10 * FAKE, dv=12 * FAKE, B=1, H=1, N=16, d=64, scale=0.125,
+             causal=1, dtype=1, grad_dtype=1, workspace=14 * FAKE, workspace_bytes=4096,
+             stream=None)
+    assert _lib.fa_bwd_phase(3, **a) == 1
+    assert _lib.fa_bwd_phase(-1, **a) == 1
+    a["workspace"] = 0
+    assert _lib.fa_bwd_phase(1, **a) == 1

@@ -170,3 +170,20 @@ def test_backward_bounded_wait_self_test():
     assert st == _lib.FA_ERR_TIMEOUT
     dq, dk, dv = api.backward(q, k, v, o, lse, do, causal=True)
     assert api.sync_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_phases_in_order_equal_fa_bwd(dtype):
+    """fa_bwd_phase(0), (1), (2) on one stream give fa_bwd's outputs bit for bit."""
+    torch = require_gpu()
+    from exact_attention_fwd_gb300 import api
+    inp = make(1, 3, 300, 64, dtype, 9940)
+    a = run_fwd_bwd(inp, causal=True)
+    ws = api.workspace(inp.B, inp.H, inp.N, a["q"].device)
+    dq, dk, dv = (torch.empty_like(a["dq"]) for _ in range(3))
+    for ph in range(3):
+        api.backward(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], causal=True, ws=ws,
+                     dq=dq, dk=dk, dv=dv, phase=ph)
+    assert api.sync_status() == 0
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.equal(a[n], t), n
