@@ -15,7 +15,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = ran
 FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F16 = range(3)
 
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_phase", "fa_bwd_workspace_size", "fa_sync_status",
-           "fa_status_string")
+           "fa_status_string", "fa_bwd_noalloc")
+FA_BWD_NOALLOC_MAX_ROWS = 1 << 22
 
 _lib = None
 
@@ -42,6 +43,8 @@ def load():
     lib.fa_bwd.restype = i
     lib.fa_bwd_phase.argtypes = [i] + lib.fa_bwd.argtypes
     lib.fa_bwd_phase.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp]
+    lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i]
     lib.fa_bwd_workspace_size.restype = sz
     lib.fa_sync_status.argtypes = [vp]
@@ -73,6 +76,13 @@ def fa_bwd_phase(phase, q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, caus
     return load().fa_bwd_phase(int(phase), q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d,
                                float(scale), int(causal), int(dtype), int(grad_dtype), workspace,
                                workspace_bytes, stream)
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, dtype,
+                   grad_dtype, stream):
+    """fa_bwd with the library's fixed device scratch instead of a workspace."""
+    return load().fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, float(scale),
+                                 int(causal), int(dtype), int(grad_dtype), stream)
 
 
 def fa_bwd_workspace_size(B, H, N):

@@ -138,6 +138,31 @@ fa_status fa_bwd_phase(int phase, const void* q, const void* k, const void* v, c
  */
 fa_status fa_sync_status(void* stream);
 
+/*
+ * fa_bwd_noalloc — fa_bwd without a workspace argument, for callers that
+ * must not allocate device memory at call time (for example code whose
+ * device memory belongs to a host framework's pool, or a latency-critical
+ * path that cannot afford cudaMalloc).  The pages have no counterpart: this
+ * is a convenience of this library.
+ *
+ * The D scratch is a fixed array of FA_BWD_NOALLOC_MAX_ROWS floats (16 MiB)
+ * inside the library's device image, present on every GPU that loads the
+ * library until the process exits.  Calls with B*H*N above that return
+ * FA_ERR_UNSUPPORTED and launch nothing.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device
+ * current), so make that first call before any stream capture.  All calls on
+ * a device share the array: calls whose GPU work overlaps (other streams,
+ * unordered host threads) race on it and produce wrong gradients.  No call
+ * allocates device memory.  Otherwise arguments, results and errors are
+ * those of fa_bwd.
+ */
+#define FA_BWD_NOALLOC_MAX_ROWS (1u << 22)
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO,
+                         void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, float scale, int causal,
+                         fa_dtype dtype, fa_dtype grad_dtype, void* stream);
+
 /* fa_status_string — static, human-readable name of a status code. */
 const char* fa_status_string(fa_status s);
 
