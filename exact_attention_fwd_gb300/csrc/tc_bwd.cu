@@ -199,12 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = p.N, H = p.H;
   const int ntiles = (N + kRows - 1) / kRows;
   const int nblocks = (N + kBlk - 1) / kBlk;
-  const int BH = p.B * H;
   const int item = blockIdx.x;
-  // longest first: dK/dV tiles near the start see the most queries (causal),
-  // dQ tiles near the end see the most keys
-  const int tile = kDkDv ? (item / BH) : (ntiles - 1 - item / BH);
-  const int bh = item % BH, b = bh / H, h = bh % H;
+  // Head-major order (the CTAs of one head share its streamed tiles through
+  // L2); within a head the longest tile first: dK/dV tiles near the start see
+  // the most queries (causal), dQ tiles near the end see the most keys.
+  const int tile = kDkDv ? (item % ntiles) : (ntiles - 1 - item % ntiles);
+  const int bh = item / ntiles, b = bh / H, h = bh % H;
   const int row0 = tile * kRows;
   int i0, i1;  // streamed blocks [i0, i1)
   if (kDkDv) {

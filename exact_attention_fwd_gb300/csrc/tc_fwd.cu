@@ -103,10 +103,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nq = (N + kBM - 1) / kBM;           // Q tiles per head
   const int nk = (N + kBN - 1) / kBN;           // K blocks per head
   const int nqp = (nq + kQT - 1) / kQT;         // Q-tile pairs per head
-  const int BH = p.B * H;
+  // Head-major order: the CTAs of one head run side by side and share its K/V
+  // through L2; within a head the longest (causal) tile pair goes first.
   const int item = blockIdx.x;
-  const int qp = nqp - 1 - item / BH;
-  const int bh = item % BH, b = bh / H, h = bh % H;
+  const int qp = nqp - 1 - item % nqp;
+  const int bh = item / nqp, b = bh / H, h = bh % H;
   const int qt0 = qp * kQT;
   const int n_active = min(kQT, nq - qt0);
   int nblk[kQT];
