@@ -296,56 +296,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (run && warp == 1) {
-    // ======================= MMA issuer =======================
-    if (lane == 0) {
+    // ============ MMA issuer (whole warp converged, lane 0 issues) ============
+    {
+      const uint32_t leader = (lane == 0) ? 1u : 0u;
       constexpr uint32_t kIdescSP = idesc_bf16(kRows, kBlk, false, false);
       constexpr uint32_t kIdescAccBf = idesc_bf16(kRows, DP, false, true);
       constexpr uint32_t kIdescAccH = idesc_f16(kRows, DP, false, true);
       const int nks = (p.d + 15) / 16;
-      const uint32_t r1a = smem_u32(sR1), r2a = smem_u32(sR2);
-      bool ok = mbar_wait(&bars->r_full, 0, abort_flag, kWaitBudget);
+      // descriptor bases; offsets advance the 16-byte start-address field
+      const uint64_t dR1 = sdesc_sw128(smem_u32(sR1), 16, 1024);
+      const uint64_t dR2 = sdesc_sw128(smem_u32(sR2), 16, 1024);
+      const uint64_t dC1 = sdesc_sw128(smem_u32(stage_c1(0)), 16, 1024);
+      const uint64_t dC2 = sdesc_sw128(smem_u32(stage_c2(0)), 16, 1024);
+      const uint64_t dC1hMN = sdesc_sw128(smem_u32(stage_c1h(0)), Cfg::kBlkChunk, 1024);
+      const uint64_t dC2MN = sdesc_sw128(smem_u32(stage_c2(0)), Cfg::kBlkChunk, 1024);
+      bool ok = warp_wait(&bars->r_full, 0, abort_flag, kWaitBudget);
 
       auto issue_sp = [&](int t) {
         const int s = t % kStages, buf = t & 1;
-        const uint32_t c1a = smem_u32(stage_c1(s)), c2a = smem_u32(stage_c2(s));
+        const uint64_t so = static_cast<uint64_t>((s * Cfg::kStageBytes) >> 4);
         for (int kk = 0; kk < nks; ++kk) {
-          const uint32_t ro = (kk >> 2) * Cfg::kRowChunk + (kk & 3) * 32;
-          const uint32_t co = (kk >> 2) * Cfg::kBlkChunk + (kk & 3) * 32;
-          mma_ss(tmem + Cfg::kTS + buf * kBlk, sdesc_sw128(r1a + ro, 16, 1024),
-                 sdesc_sw128(c1a + co, 16, 1024), kIdescSP, kk > 0);
-          mma_ss(tmem + Cfg::kTdP + buf * kBlk, sdesc_sw128(r2a + ro, 16, 1024),
-                 sdesc_sw128(c2a + co, 16, 1024), kIdescSP, kk > 0);
+          const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * Cfg::kRowChunk + (kk & 3) * 32) >> 4);
+          const uint64_t co = static_cast<uint64_t>(((kk >> 2) * Cfg::kBlkChunk + (kk & 3) * 32) >> 4);
+          mma_ss_w(tmem + Cfg::kTS + buf * kBlk, dR1 + ro, dC1 + so + co, kIdescSP, kk > 0, leader);
+          mma_ss_w(tmem + Cfg::kTdP + buf * kBlk, dR2 + ro, dC2 + so + co, kIdescSP, kk > 0,
+                   leader);
         }
-        mma_commit(&bars->s_full[buf]);
+        mma_commit_w(&bars->s_full[buf], leader);
       };
       auto issue_acc = [&](int t) {
         const int s = t % kStages, buf = t & 1;
-        const uint32_t c1h = smem_u32(stage_c1h(s)), c2a = smem_u32(stage_c2(s));
+        const uint64_t so = static_cast<uint64_t>((s * Cfg::kStageBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk) {
           const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
           const uint32_t pa = tmem + Cfg::kTS + buf * kBlk + kk * 8;    // P
           const uint32_t da = tmem + Cfg::kTdP + buf * kBlk + kk * 8;   // dS
+          const uint64_t ko = static_cast<uint64_t>((kk * 2048) >> 4);
           if (kDkDv)  // dV += P dO_i (bf16)
-            mma_ts(tmem + Cfg::kTAcc1, pa, sdesc_sw128(c2a + kk * 2048, Cfg::kBlkChunk, 1024),
-                   kIdescAccBf, acc);
+            mma_ts_w(tmem + Cfg::kTAcc1, pa, dC2MN + so + ko, kIdescAccBf, acc, leader);
           else        // B += P K_j (fp16)
-            mma_ts(tmem + Cfg::kTAcc1, pa, sdesc_sw128(c1h + kk * 2048, Cfg::kBlkChunk, 1024),
-                   kIdescAccH, acc);
+            mma_ts_w(tmem + Cfg::kTAcc1, pa, dC1hMN + so + ko, kIdescAccH, acc, leader);
           // dK += dS Q_i   or   dQ += dS K_j   (fp16)
-          mma_ts(tmem + Cfg::kTAcc2, da, sdesc_sw128(c1h + kk * 2048, Cfg::kBlkChunk, 1024),
-                 kIdescAccH, acc);
+          mma_ts_w(tmem + Cfg::kTAcc2, da, dC1hMN + so + ko, kIdescAccH, acc, leader);
         }
-        mma_commit(&bars->c_empty[s]);
+        mma_commit_w(&bars->c_empty[s], leader);
       };
       auto ready_acc = [&](int t) {
-        return mbar_wait(&bars->p_full[t & 1], (t >> 1) & 1, abort_flag, kWaitBudget) &&
-               mbar_wait(&bars->conv_full[t % kStages], (t / kStages) & 1, abort_flag,
+        return warp_wait(&bars->p_full[t & 1], (t >> 1) & 1, abort_flag, kWaitBudget) &&
+               warp_wait(&bars->conv_full[t % kStages], (t / kStages) & 1, abort_flag,
                          kWaitBudget);
       };
 
       for (int t = 0; t < nb && ok; ++t) {
-        if (!mbar_wait(&bars->c_full[t % kStages], (t / kStages) & 1, abort_flag, kWaitBudget)) {
+        if (!warp_wait(&bars->c_full[t % kStages], (t / kStages) & 1, abort_flag, kWaitBudget)) {
           ok = false;
           break;
         }
@@ -364,13 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ready_acc(nb - 1)) {
           tc_fence_after();
           issue_acc(nb - 1);
-          mma_commit(&bars->acc_full);
+          mma_commit_w(&bars->acc_full, leader);
         } else {
           ok = false;
         }
       }
-      if (!ok) raise_abort(bars, p.status);
-      mma_commit(&bars->drain);
+      if (!ok && leader) raise_abort(bars, p.status);
+      mma_commit_w(&bars->drain, leader);
       mbar_wait(&bars->drain, 0, nullptr, kDrainBudget);
     }
     __syncwarp();

@@ -6,24 +6,33 @@
 // keeps the online-softmax state (m, l, O) so the N x N scores never reach
 // global memory; the per-row log-sum-exp L = m + log l is written at the end.
 //
-// GB300 mapping (one CTA per SM, 12 warps):
-//   * a CTA owns two adjacent 128-row Q tiles of one (b, h); both tiles share
-//     every K/V block it loads, which halves K/V traffic into shared memory;
-//   * warp 0 (one lane) issues TMA tile loads: Q once, then K_j and V_j into a
-//     ring of shared-memory stages guarded by full/empty mbarriers;
+// GB300 mapping: a persistent kernel, one CTA per SM, 12 warps.
+//   * Work item = two 128-row Q tiles of one (b, h).  With the causal mask the
+//     pair is (i, nq-1-i): tile i sees i+1 key blocks and tile nq-1-i sees
+//     nq-i, so every item has the same nq+1 block-tiles of work and a static
+//     round-robin schedule is balanced.  Items are numbered head-major, so the
+//     CTAs working at one time share a few heads' K/V through L2.  Both tiles
+//     share every K/V block they both need.
+//   * warp 0 (one lane) issues TMA tile loads: the item's Q tiles, then K_j
+//     and V_j into a ring of shared-memory stages guarded by full/empty
+//     mbarriers.  The ring's position and every barrier's phase carry over
+//     from item to item, so the next item's loads overlap this item's tail.
 //   * warp 1 (one lane) issues tcgen05 MMAs: S_g = Q_g K_j^T (both operands
 //     K-major in smem, fp32 accumulator in TMEM) and O_g += P_g V_j (P read
-//     from TMEM, V as an MN-major smem operand).  MMAs of the two Q tiles
-//     interleave so one tile's softmax overlaps the other tile's MMAs;
-//   * warps 4-7 and 8-11 are the softmax warpgroups of Q tiles 0 and 1: one
+//     from TMEM, V as an MN-major smem operand).  The two tiles' MMAs
+//     interleave, so one tile's softmax overlaps the other tile's MMAs.
+//   * warps 4-7 and 8-11 are the softmax warpgroups of tiles 0 and 1: one
 //     thread per query row (= TMEM lane) loads its row of S, masks, takes the
 //     row max, exponentiates in base 2 with scale*log2(e) folded in, writes P
 //     as bf16 back into the same TMEM columns, and keeps m and l in registers.
-//     The output is rescaled by alpha = 2^(m_old - m_new) in TMEM only when the
-//     running max rises by more than kRescaleThreshold (log2 units); a stale
-//     reference max cancels exactly in O / l and in L.
-//   * after the last block each softmax thread divides its O row by l, rounds
-//     once to bf16 and stores it, and stores L in natural-log units.
+//     O is rescaled by alpha = 2^(m_old - m_new) in TMEM only when the running
+//     max rises by more than kRescaleThreshold (log2 units); a stale reference
+//     max cancels exactly in O / l and in L.  After an item's last block each
+//     thread divides its O row by l, rounds once to bf16 and stores it, and
+//     stores L in natural-log units; meanwhile the MMA warp already computes
+//     the next item's first scores.
+//   * the producer/MMA warpgroup gives registers to the softmax warpgroups
+//     (setmaxnreg), which hold a full 128-score row per thread.
 //
 // Tiles are stored in shared memory as 64-column (128-byte) chunks with the
 // 128-byte swizzle; head dims below the padded width DP are zero-filled by
@@ -38,7 +47,6 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
-#include <mutex>
 
 #include "fa_common.cuh"
 #include "sm103_ptx.cuh"
@@ -49,14 +57,25 @@ namespace {
 
 constexpr int kBM = 128;                 // query rows per Q tile (= TMEM lanes)
 constexpr int kBN = 128;                 // keys per K/V block
-constexpr int kQT = 2;                   // Q tiles per CTA
+constexpr int kQT = 2;                   // Q tiles per work item
 constexpr int kThreads = 384;            // 12 warps
 constexpr int kChunkBytes = kBM * 128;   // one 64-column swizzled chunk of 128 rows
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kRegsLoad = 64;            // warps 0-3 (TMA, MMA, idle)
+constexpr int kRegsSoftmax = 216;        // warps 4-11
+static_assert(4 * 32 * kRegsLoad + 8 * 32 * kRegsSoftmax <= 168 * kThreads,
+              "register split exceeds the launch allocation");
 
+// TMEM columns.  S_g: [128 g, 128 g + 128).  O_g: [256 + DP g, 256 + DP g + DP).
+// With DP = 64 the 128 columns left over hold P_g (bf16 pairs) at
+// [384 + 64 g, 448 + 64 g), so the next S of a tile can be computed while its
+// softmax still works on the current block and the previous PV overlaps the
+// next softmax.  With DP = 128 TMEM is full and P_g is written over the first
+// 64 columns of S_g, so a tile's next S waits until its PV has been issued.
 template <int DP>
 struct FwdCfg {
+  static constexpr bool kSepP = (DP == 64);
   static constexpr int kChunks = DP / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kStages = (DP == 64) ? 4 : 2;
@@ -68,12 +87,15 @@ struct FwdCfg {
 };
 
 struct FwdBars {
-  uint64_t q_full[kQT];
+  uint64_t q_full;
+  uint64_t q_empty;
   uint64_t k_full[4];
   uint64_t v_full[4];
   uint64_t kv_empty[4];
   uint64_t s_full[kQT];
+  uint64_t s_free[kQT];    // softmax has loaded S (separate-P layout)
   uint64_t p_full[kQT];
+  uint64_t pv_done[kQT];   // O += P V of a block has completed (separate-P layout)
   uint64_t o_final[kQT];
   uint64_t drain;
   uint64_t probe;
@@ -86,11 +108,60 @@ __device__ __forceinline__ void raise_abort(FwdBars* bars, int* status) {
   *reinterpret_cast<volatile int*>(&bars->abort) = 1;
 }
 
+// Bounded wait with a warp-uniform outcome (for roles run by a whole warp).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* ab,
+                                          long long budget) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, budget));
+}
+
+// Work item -> (b, h) and its two adjacent Q tiles (2p, 2p+1); tile[0] is the
+// later, longer one under the causal mask.  The two tiles' softmax
+// warpgroups are both busy for all but the last block, so their MMAs and
+// exponentials interleave.
+struct Item {
+  int b, h;
+  int tile[kQT];   // Q tile index, or -1
+  int nblk[kQT];   // K blocks each tile visits
+  int nmax;
+};
+
+template <bool kCausal>
+__device__ __forceinline__ Item decode_item(int it, int nq, int nk, int H) {
+  const int npairs = (nq + 1) / 2;
+  const int bh = it / npairs, pr = it % npairs;
+  Item r;
+  r.b = bh / H;
+  r.h = bh % H;
+  const int lo = 2 * pr, hi = 2 * pr + 1;
+  r.tile[0] = (hi < nq) ? hi : lo;
+  r.tile[1] = (hi < nq) ? lo : -1;
+#pragma unroll
+  for (int g = 0; g < kQT; ++g)
+    r.nblk[g] = (r.tile[g] < 0) ? 0 : (kCausal ? min(nk, r.tile[g] + 1) : nk);
+  r.nmax = max(r.nblk[0], r.nblk[1]);
+  return r;
+}
+
+// Static schedule: the li-th item of this CTA.  Wave li covers items
+// [li*G, (li+1)*G) (G = grid size), so the CTAs working at one time share a
+// few heads; odd full waves run in reverse CTA order, which pairs a CTA's
+// short causal items with long ones (with G a multiple of the items per head,
+// a CTA alternates between complementary tile pairs).  Returns -1 when done.
+__device__ __forceinline__ int item_index(int li, int num_items) {
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long base = static_cast<long long>(li) * G;
+  if (base >= num_items) return -1;
+  const bool reverse = (li & 1) && base + G <= num_items;
+  const long long it = base + (reverse ? G - 1 - c : c);
+  return it < num_items ? static_cast<int>(it) : -1;
+}
+
 template <int DP, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using Cfg = FwdCfg<DP>;
+  constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -98,34 +169,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
 
-  // ---- work item: two adjacent Q tiles of one (b, h); longest rows first ----
   const int N = p.N, H = p.H;
   const int nq = (N + kBM - 1) / kBM;           // Q tiles per head
   const int nk = (N + kBN - 1) / kBN;           // K blocks per head
-  const int nqp = (nq + kQT - 1) / kQT;         // Q-tile pairs per head
-  // Head-major order: the CTAs of one head run side by side and share its K/V
-  // through L2; within a head the longest (causal) tile pair goes first.
-  const int item = blockIdx.x;
-  const int qp = nqp - 1 - item % nqp;
-  const int bh = item / nqp, b = bh / H, h = bh % H;
-  const int qt0 = qp * kQT;
-  const int n_active = min(kQT, nq - qt0);
-  int nblk[kQT];
-#pragma unroll
-  for (int g = 0; g < kQT; ++g)
-    nblk[g] = (g < n_active) ? (kCausal ? min(nk, qt0 + g + 1) : nk) : 0;
-  const int nmax = max(nblk[0], nblk[1]);
+  const int num_items = ((nq + 1) / 2) * p.B * H;
 
   // ---- setup: barriers, TMEM ----
   if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
 #pragma unroll
     for (int g = 0; g < kQT; ++g) {
-      mbar_init(&bars->q_full[g], 1);
       mbar_init(&bars->s_full[g], 1);
+      mbar_init(&bars->s_free[g], kBM);
       mbar_init(&bars->p_full[g], kBM);
+      mbar_init(&bars->pv_done[g], 1);
       mbar_init(&bars->o_final[g], 1);
     }
-    for (int s = 0; s < Cfg::kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
@@ -157,142 +218,241 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + Cfg::kKOff;
   uint8_t* sV = smem + Cfg::kVOff;
 
-  if (run && warp == 0) {
+  // Role bodies; each runs inside the branch that sets its register budget.
+  auto load_roles = [&](int warp, int lane) {
+    if (warp == 0) {
     // ======================= TMA producer =======================
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      for (int g = 0; g < n_active; ++g) {
-        mbar_arrive_expect_tx(&bars->q_full[g], Cfg::kTileBytes);
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_4d(sQ + g * Cfg::kTileBytes + c * kChunkBytes, &tmQ, &bars->q_full[g], c * 64,
-                      h, (qt0 + g) * kBM, b);
-      }
-      int issued = 0;
-      for (int j = 0; j < nmax; ++j) {
-        const int s = j % Cfg::kStages, round = j / Cfg::kStages;
-        if (round > 0 && !mbar_wait(&bars->kv_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
-          raise_abort(bars, p.status);
-          break;
-        }
-        mbar_arrive_expect_tx(&bars->k_full[s], Cfg::kTileBytes);
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_4d(sK + s * Cfg::kTileBytes + c * kChunkBytes, &tmK, &bars->k_full[s], c * 64, h,
-                      j * kBN, b);
-        mbar_arrive_expect_tx(&bars->v_full[s], Cfg::kTileBytes);
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_4d(sV + s * Cfg::kTileBytes + c * kChunkBytes, &tmV, &bars->v_full[s], c * 64, h,
-                      j * kBN, b);
-        issued = j + 1;
-      }
-      // Drain: every issued copy has landed before the CTA may exit.
-      for (int j = max(0, issued - Cfg::kStages); j < issued; ++j) {
-        const int s = j % Cfg::kStages, par = (j / Cfg::kStages) & 1;
-        mbar_wait(&bars->k_full[s], par, nullptr, kDrainBudget);
-        mbar_wait(&bars->v_full[s], par, nullptr, kDrainBudget);
-      }
-      for (int g = 0; g < n_active; ++g) mbar_wait(&bars->q_full[g], 0, nullptr, kDrainBudget);
-    }
-    __syncwarp();
-  } else if (run && warp == 1) {
-    // ======================= MMA issuer =======================
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16(kBM, DP, false, true);
-      const int nks = (p.d + 15) / 16;       // K=16 steps over the head dim
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      int c = 0;        // K/V blocks issued so far
+      int li = 0;       // items started by this CTA
       bool ok = true;
-
-      auto issue_s = [&](int g, int j) {
-        const int s = j % Cfg::kStages;
-        const uint32_t qa = sQa + g * Cfg::kTileBytes;
-        const uint32_t ka = sKa + s * Cfg::kTileBytes;
-        for (int kk = 0; kk < nks; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + g * kBN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 kIdescQK, kk > 0);
-        }
-        mma_commit(&bars->s_full[g]);
-      };
-      auto issue_pv = [&](int g, int j) {
-        const int s = j % Cfg::kStages;
-        const uint32_t va = sVa + s * Cfg::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + 2 * kBN + g * DP, tmem + g * kBN + kk * 8,
-                 sdesc_sw128(va + kk * 2048, kChunkBytes, 1024), kIdescPV, (j > 0 || kk > 0));
-      };
-
-      for (int g = 0; g < n_active && ok; ++g)
-        if (!mbar_wait(&bars->q_full[g], 0, abort_flag, kWaitBudget)) ok = false;
-      if (ok && !mbar_wait(&bars->k_full[0], 0, abort_flag, kWaitBudget)) ok = false;
-      if (ok) {
-        tc_fence_after();
-        for (int g = 0; g < n_active; ++g) issue_s(g, 0);
-      }
-      for (int j = 0; j < nmax && ok; ++j) {
-        const int s = j % Cfg::kStages;
-        if (!mbar_wait(&bars->v_full[s], (j / Cfg::kStages) & 1, abort_flag, kWaitBudget)) {
+      for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(li, num_items)) {
+        const Item w = decode_item<kCausal>(it, nq, nk, H);
+        if (li > 0 && !mbar_wait(&bars->q_empty, (li - 1) & 1, abort_flag, kWaitBudget)) {
           ok = false;
           break;
         }
-        bool k_next = false;
-        for (int g = 0; g < kQT; ++g) {
-          if (j >= nblk[g]) continue;
-          if (!mbar_wait(&bars->p_full[g], j & 1, abort_flag, kWaitBudget)) {
+        const int nact = (w.tile[1] < 0) ? 1 : 2;
+        mbar_arrive_expect_tx(&bars->q_full, nact * Cfg::kTileBytes);
+        for (int g = 0; g < nact; ++g)
+          for (int ch = 0; ch < Cfg::kChunks; ++ch)
+            tma_load_4d(sQ + g * Cfg::kTileBytes + ch * kChunkBytes, &tmQ, &bars->q_full, ch * 64,
+                        w.h, w.tile[g] * kBM, w.b);
+        ++li;
+        for (int j = 0; j < w.nmax; ++j) {
+          const int s = c % S, round = c / S;
+          if (round > 0 &&
+              !mbar_wait(&bars->kv_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->k_full[s], Cfg::kTileBytes);
+          for (int ch = 0; ch < Cfg::kChunks; ++ch)
+            tma_load_4d(sK + s * Cfg::kTileBytes + ch * kChunkBytes, &tmK, &bars->k_full[s],
+                        ch * 64, w.h, j * kBN, w.b);
+          mbar_arrive_expect_tx(&bars->v_full[s], Cfg::kTileBytes);
+          for (int ch = 0; ch < Cfg::kChunks; ++ch)
+            tma_load_4d(sV + s * Cfg::kTileBytes + ch * kChunkBytes, &tmV, &bars->v_full[s],
+                        ch * 64, w.h, j * kBN, w.b);
+          ++c;
+        }
+      }
+      if (!ok) raise_abort(bars, p.status);
+      // Drain: every issued copy has landed before the CTA may exit.  c counts
+      // the K/V blocks issued; li the Q loads (phase li-1 of q_full is last).
+      for (int x = max(0, c - S); x < c; ++x) {
+        mbar_wait(&bars->k_full[x % S], (x / S) & 1, nullptr, kDrainBudget);
+        mbar_wait(&bars->v_full[x % S], (x / S) & 1, nullptr, kDrainBudget);
+      }
+      if (li > 0) mbar_wait(&bars->q_full, (li - 1) & 1, nullptr, kDrainBudget);
+    }
+    __syncwarp();
+    } else if (warp == 1) {
+    // ======================= MMA issuer (whole warp, lane 0 issues) =======================
+    {
+      const uint32_t leader = (lane == 0) ? 1u : 0u;
+      constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(kBM, DP, false, true);
+      const int nks = (p.d + 15) / 16;       // K=16 steps over the head dim
+      // Descriptor bases; K steps and stages advance the start-address field.
+      const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(sV), kChunkBytes, 1024);
+      auto kstep = [](int kk) -> uint64_t {
+        return static_cast<uint64_t>(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
+      };
+      auto issue_s = [&](int g, int s) {
+        const uint64_t qa = dQ + ((g * Cfg::kTileBytes) >> 4);
+        const uint64_t ka = dK + ((s * Cfg::kTileBytes) >> 4);
+        for (int kk = 0; kk < nks; ++kk)
+          mma_ss_w(tmem + g * kBN, qa + kstep(kk), ka + kstep(kk), kIdescQK, kk > 0, leader);
+        mma_commit_w(&bars->s_full[g], leader);
+      };
+      auto issue_pv = [&](int g, int s, bool acc) {
+        const uint64_t va = dV + ((s * Cfg::kTileBytes) >> 4);
+        const uint32_t pa = Cfg::kSepP ? tmem + 384 + g * 64 : tmem + g * kBN;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts_w(tmem + 2 * kBN + g * DP, pa + kk * 8, va + ((kk * 2048) >> 4), kIdescPV,
+                   (acc || kk > 0) ? 1u : 0u, leader);
+      };
+
+      int c = 0;                 // K/V blocks consumed so far (same count as the producer)
+      int pc[kQT] = {0, 0};      // p_full phases consumed per tile
+      int sk[kQT] = {0, 0};      // S MMAs issued per tile (separate-P layout)
+      int li = 0;
+      bool ok = true;
+      if constexpr (Cfg::kSepP) {
+        // S of a tile's block j+1 goes out as soon as its softmax has loaded S
+        // of block j; O += P V of block j as soon as P of block j is ready.
+        auto next_s = [&](int g, int s) -> bool {
+          if (sk[g] > 0 && !warp_wait(&bars->s_free[g], (sk[g] - 1) & 1, abort_flag, kWaitBudget))
+            return false;
+          tc_fence_after();
+          issue_s(g, s);
+          ++sk[g];
+          return true;
+        };
+        for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
+          const Item w = decode_item<kCausal>(it, nq, nk, H);
+          if (!warp_wait(&bars->q_full, li & 1, abort_flag, kWaitBudget) ||
+              !warp_wait(&bars->k_full[c % S], (c / S) & 1, abort_flag, kWaitBudget)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(g, j);
-          if (j + 1 < nblk[g]) {
-            if (!k_next) {
-              const int s1 = (j + 1) % Cfg::kStages;
-              if (!mbar_wait(&bars->k_full[s1], ((j + 1) / Cfg::kStages) & 1, abort_flag,
+          for (int g = 0; g < kQT && ok; ++g)
+            if (w.nblk[g] > 0 && !next_s(g, c % S)) ok = false;
+          for (int j = 0; j < w.nmax && ok; ++j) {
+            const int cj = c + j, s = cj % S;
+            if (j + 1 < w.nmax) {
+              if (!warp_wait(&bars->k_full[(cj + 1) % S], ((cj + 1) / S) & 1, abort_flag,
                              kWaitBudget)) {
                 ok = false;
                 break;
               }
-              tc_fence_after();
-              k_next = true;
+              for (int g = 0; g < kQT && ok; ++g)
+                if (j + 1 < w.nblk[g] && !next_s(g, (cj + 1) % S)) ok = false;
+              if (!ok) break;
+            } else {
+              // every score MMA of this item has been issued: once they
+              // complete, the producer may load the next item's Q tiles
+              mma_commit_w(&bars->q_empty, leader);
             }
-            issue_s(g, j + 1);
-          } else {
-            mma_commit(&bars->o_final[g]);
+            if (!warp_wait(&bars->v_full[s], (cj / S) & 1, abort_flag, kWaitBudget)) {
+              ok = false;
+              break;
+            }
+            for (int g = 0; g < kQT; ++g) {
+              if (j >= w.nblk[g]) continue;
+              if (!warp_wait(&bars->p_full[g], pc[g] & 1, abort_flag, kWaitBudget)) {
+                ok = false;
+                break;
+              }
+              ++pc[g];
+              tc_fence_after();
+              issue_pv(g, s, j > 0);
+              mma_commit_w(&bars->pv_done[g], leader);
+              if (j == w.nblk[g] - 1) mma_commit_w(&bars->o_final[g], leader);
+            }
+            if (!ok) break;
+            mma_commit_w(&bars->kv_empty[s], leader);
           }
+          c += w.nmax;
         }
-        if (!ok) break;
-        mma_commit(&bars->kv_empty[s]);
+      } else {
+        for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
+          const Item w = decode_item<kCausal>(it, nq, nk, H);
+          if (!warp_wait(&bars->q_full, li & 1, abort_flag, kWaitBudget) ||
+              !warp_wait(&bars->k_full[c % S], (c / S) & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int g = 0; g < kQT; ++g)
+            if (w.nblk[g] > 0) issue_s(g, c % S);
+          for (int j = 0; j < w.nmax; ++j) {
+            const int cj = c + j, s = cj % S;
+            if (!warp_wait(&bars->v_full[s], (cj / S) & 1, abort_flag, kWaitBudget)) {
+              ok = false;
+              break;
+            }
+            // Every score MMA of this item has been issued by now: once they
+            // complete, the producer may load the next item's Q tiles.
+            if (j == w.nmax - 1) mma_commit_w(&bars->q_empty, leader);
+            bool k_next = false;
+            for (int g = 0; g < kQT; ++g) {
+              if (j >= w.nblk[g]) continue;
+              if (!warp_wait(&bars->p_full[g], pc[g] & 1, abort_flag, kWaitBudget)) {
+                ok = false;
+                break;
+              }
+              ++pc[g];
+              tc_fence_after();
+              issue_pv(g, s, j > 0);
+              if (j + 1 < w.nblk[g]) {
+                if (!k_next) {
+                  if (!warp_wait(&bars->k_full[(cj + 1) % S], ((cj + 1) / S) & 1, abort_flag,
+                                 kWaitBudget)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  k_next = true;
+                }
+                issue_s(g, (cj + 1) % S);
+              } else {
+                mma_commit_w(&bars->o_final[g], leader);
+              }
+            }
+            if (!ok) break;
+            mma_commit_w(&bars->kv_empty[s], leader);
+          }
+          c += w.nmax;
+        }
+
       }
-      if (!ok) raise_abort(bars, p.status);
+      if (!ok && leader) raise_abort(bars, p.status);
       // Drain: no MMA may be in flight when TMEM is released.
-      mma_commit(&bars->drain);
+      mma_commit_w(&bars->drain, leader);
       mbar_wait(&bars->drain, 0, nullptr, kDrainBudget);
     }
     __syncwarp();
-  } else if (run && warp >= 4) {
+    }
+  };
+  auto softmax_role = [&]() {
     // ======================= softmax warpgroups =======================
     const int g = (warp - 4) / 4;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int qt = qt0 + g;
-    const int q_row = qt * kBM + row;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + g * kBN;
     const uint32_t tO = tmem + lane_base + 2 * kBN + g * DP;
+    const uint32_t tP = tmem + lane_base + 384 + g * 64;   // separate-P layout only
     const float c = p.scale_log2;
-    float m_ref = -INFINITY;   // reference max of the scaled scores, log2 units
-    float l = 0.0f;
+    int sc = 0;    // s_full phases consumed
+    int oc = 0;    // o_final phases consumed
     bool ok = true;
 
-    if (g < n_active) {
-      for (int j = 0; j < nblk[g]; ++j) {
+    int li = 0;
+    for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
+      const Item w = decode_item<kCausal>(it, nq, nk, H);
+      const int qt = w.tile[g];
+      if (qt < 0) continue;
+      const int q_row = qt * kBM + row;
+      float m_ref = -INFINITY;   // reference max of the scaled scores, log2 units
+      float l = 0.0f;
+      for (int j = 0; j < w.nblk[g]; ++j) {
         // warp-uniform outcome: the TMEM accesses below are warp-collective
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[g], j & 1, abort_flag, kWaitBudget))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[g], sc & 1, abort_flag,
+                                               kWaitBudget))) {
           ok = false;
           break;
         }
+        ++sc;
         tc_fence_after();
         uint32_t sr[kBN];
         tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
@@ -300,38 +460,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
         tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
         tmem_ld_wait(sr);
-        float* s = reinterpret_cast<float*>(sr);
+        // a float copy (registers): writing floats through a pointer into the
+        // uint32 array would break type-based aliasing rules
+        float s[kBN];
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sr[i]);
+        if constexpr (Cfg::kSepP) {
+          // S is in registers: its TMEM columns may take the next block's S
+          tc_fence_before();
+          mbar_arrive(&bars->s_free[g]);
+        }
 
+        // One code path for every block (the instruction cache holds one copy
+        // of the unrolled row loops): blocks with masked keys, and the rare
+        // non-positive scale, first scale the row in place and set masked
+        // keys to -inf; the common case folds the scale into the exponent.
         const bool masked = (kCausal && j == qt) || ((j + 1) * kBN > N);
-        float m_blk;
-        if (masked) {
+        float c_eff = c;
+        if (masked || !(c > 0.0f)) {
           const int k0 = j * kBN;
-          float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
           for (int i = 0; i < kBN; ++i) {
-            const int key = k0 + i;
-            const bool bad = (key >= N) || (kCausal && key > q_row);
+            const bool bad = (k0 + i >= N) || (kCausal && k0 + i > q_row);
             s[i] = bad ? -INFINITY : s[i] * c;
-            if (i & 1) mx1 = fmaxf(mx1, s[i]); else mx0 = fmaxf(mx0, s[i]);
           }
-          m_blk = fmaxf(mx0, mx1);
-        } else {
-          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
-          if (c >= 0.0f) {
+          c_eff = 1.0f;
+        }
+        float m_blk;
+        {
+          float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-            for (int i = 4; i < kBN; i += 4) {
-              a0 = fmaxf(a0, s[i]); a1 = fmaxf(a1, s[i + 1]);
-              a2 = fmaxf(a2, s[i + 2]); a3 = fmaxf(a3, s[i + 3]);
-            }
-            m_blk = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c;
-          } else {
-#pragma unroll
-            for (int i = 4; i < kBN; i += 4) {
-              a0 = fminf(a0, s[i]); a1 = fminf(a1, s[i + 1]);
-              a2 = fminf(a2, s[i + 2]); a3 = fminf(a3, s[i + 3]);
-            }
-            m_blk = fminf(fminf(a0, a1), fminf(a2, a3)) * c;
+          for (int i = 0; i < kBN; i += 8) {   // four chains, columns 0 .. kBN-1
+            a0 = fmax3(a0, s[i], s[i + 1]);
+            a1 = fmax3(a1, s[i + 2], s[i + 3]);
+            a2 = fmax3(a2, s[i + 4], s[i + 5]);
+            a3 = fmax3(a3, s[i + 6], s[i + 7]);
           }
+          m_blk = fmax3(a0, a1, fmaxf(a2, a3)) * c_eff;
         }
 
         // Lazy rescale: move the reference max only when it rises enough.
@@ -342,93 +507,125 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = (m_ref == -INFINITY) ? 0.0f : fast_exp2(m_ref - m_blk);
           m_ref = m_blk;
         }
-        if (j > 0 && __any_sync(0xffffffffu, rise)) {
-          // O row *= alpha in TMEM (PV of block j-1 has completed: s_full of
-          // block j was committed after it).
+        const bool rescale = j > 0 && __any_sync(0xffffffffu, rise);
+        // O row *= alpha in TMEM (warp-collective; alpha is 1 in rows whose
+        // max did not move).  Called once O holds every block before this one.
+        auto rescale_o = [&]() {
+          const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
           for (int cc = 0; cc < DP / 32; ++cc) {
             uint32_t orr[32];
             tmem_ld32(tO + cc * 32, orr);
             tmem_ld_wait(orr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            for (int i = 0; i < 32; i += 2) {
+              const uint64_t v = f2_mul(f2_pack(__uint_as_float(orr[i]),
+                                                __uint_as_float(orr[i + 1])), a2);
+              orr[i] = __float_as_uint(f2_lo(v));
+              orr[i + 1] = __float_as_uint(f2_hi(v));
+            }
             tmem_st32(tO + cc * 32, orr);
           }
-        }
+        };
+        // Aliased layout: PV of block j-1 has completed, since the s_full
+        // commit of block j came after it.
+        if (!Cfg::kSepP && rescale) rescale_o();
         l *= alpha;
         const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        const uint64_t ce2 = f2_pack(c_eff, c_eff);
 
-        // P = 2^(s c - m) -> bf16 pairs into TMEM columns [0, 64) of S.
-        float l0 = 0.0f, l1 = 0.0f;
+        // P = 2^(s c - m) as bf16 pairs.
+        uint64_t lsum0 = 0, lsum1 = 0;   // two packed partial sums (+0.0f pairs)
+        uint32_t pk[kBN / 2];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int e = half * 64 + 2 * i;
-            float p0, p1;
-            if (masked) {
-              p0 = fast_exp2(s[e] - m_use);
-              p1 = fast_exp2(s[e + 1] - m_use);
-            } else {
-              p0 = fast_exp2(fmaf(s[e], c, -m_use));
-              p1 = fast_exp2(fmaf(s[e + 1], c, -m_use));
-            }
-            l0 += p0;
-            l1 += p1;
-            pk[i] = pack_bf16x2(p0, p1);
-          }
-          tmem_st32(tS + half * 32, pk);
+        for (int i = 0; i < kBN / 2; ++i) {
+          const uint64_t sv = f2_pack(s[2 * i], s[2 * i + 1]);
+          const uint64_t t = f2_fma(sv, ce2, negm2);
+          const float p0 = fast_exp2(f2_lo(t));
+          const float p1 = fast_exp2(f2_hi(t));
+          const uint64_t pp = f2_pack(p0, p1);
+          if (i & 1) lsum1 = f2_add(lsum1, pp); else lsum0 = f2_add(lsum0, pp);
+          pk[i] = pack_bf16x2(p0, p1);
         }
-        l += l0 + l1;
+        const uint64_t ls = f2_add(lsum0, lsum1);
+        l += f2_lo(ls) + f2_hi(ls);
+        if constexpr (Cfg::kSepP) {
+          // P_g and O_g are free once PV of the previous block has completed
+          // (the pv_done phase of that block; blocks counted across items).
+          if (sc >= 2 &&
+              !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[g], sc & 1, abort_flag,
+                                                 kWaitBudget))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (rescale) rescale_o();
+          tmem_st32(tP + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        } else {
+          tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_full[g]);
       }
+      if (!ok) break;
 
       // ---- epilogue: O / l -> bf16, L = (m + log2 l) ln 2 ----
-      if (ok && !__all_sync(0xffffffffu, mbar_wait(&bars->o_final[g], 0, abort_flag, kWaitBudget)))
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_final[g], oc & 1, abort_flag,
+                                             kWaitBudget))) {
         ok = false;
-      if (ok) {
-        tc_fence_after();
-        const bool live = l > 0.0f;
-        const float inv = live ? 1.0f / l : 0.0f;
-        const bool store = q_row < N;
-        __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
-        uint4* orow = reinterpret_cast<uint4*>(
-            O + ((static_cast<size_t>(b) * N + (store ? q_row : 0)) * H + h) * p.d);
+        break;
+      }
+      ++oc;
+      tc_fence_after();
+      const bool live = l > 0.0f;
+      const float inv = live ? 1.0f / l : 0.0f;
+      const bool store = q_row < N;
+      __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
+      uint4* orow = reinterpret_cast<uint4*>(
+          O + ((static_cast<size_t>(w.b) * N + (store ? q_row : 0)) * H + w.h) * p.d);
 #pragma unroll
-        for (int cc = 0; cc < DP / 32; ++cc) {
-          uint32_t orr[32];
-          tmem_ld32(tO + cc * 32, orr);
-          tmem_ld_wait(orr);
-          if (store) {
+      for (int cc = 0; cc < DP / 32; ++cc) {
+        uint32_t orr[32];
+        tmem_ld32(tO + cc * 32, orr);
+        tmem_ld_wait(orr);
+        if (store) {
 #pragma unroll
-            for (int qv = 0; qv < 4; ++qv) {
-              const int col = cc * 32 + qv * 8;
-              if (col < p.d) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(orr[qv * 8 + 0]) * inv,
-                                  __uint_as_float(orr[qv * 8 + 1]) * inv);
-                v.y = pack_bf16x2(__uint_as_float(orr[qv * 8 + 2]) * inv,
-                                  __uint_as_float(orr[qv * 8 + 3]) * inv);
-                v.z = pack_bf16x2(__uint_as_float(orr[qv * 8 + 4]) * inv,
-                                  __uint_as_float(orr[qv * 8 + 5]) * inv);
-                v.w = pack_bf16x2(__uint_as_float(orr[qv * 8 + 6]) * inv,
-                                  __uint_as_float(orr[qv * 8 + 7]) * inv);
-                orow[col / 8] = v;
-              }
+          for (int qv = 0; qv < 4; ++qv) {
+            const int col = cc * 32 + qv * 8;
+            if (col < p.d) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(orr[qv * 8 + 0]) * inv,
+                                __uint_as_float(orr[qv * 8 + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(orr[qv * 8 + 2]) * inv,
+                                __uint_as_float(orr[qv * 8 + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(orr[qv * 8 + 4]) * inv,
+                                __uint_as_float(orr[qv * 8 + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(orr[qv * 8 + 6]) * inv,
+                                __uint_as_float(orr[qv * 8 + 7]) * inv);
+              orow[col / 8] = v;
             }
           }
         }
-        if (store)
-          p.lse[static_cast<size_t>(bh) * N + q_row] =
-              live ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
-      if (!ok) raise_abort(bars, p.status);
+      tc_fence_before();
+      if (store)
+        p.lse[(static_cast<size_t>(w.b) * H + w.h) * N + q_row] =
+            live ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
+    if (!ok) raise_abort(bars, p.status);
     __syncwarp();
+  };
+
+  if (warp < 4) {
+    regs_dec<kRegsLoad>();
+    if (run) load_roles(warp, lane);
+  } else {
+    regs_inc<kRegsSoftmax>();
+    if (run) softmax_role();
   }
 
   // ---- teardown ----
@@ -438,6 +635,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
 }
 
 template <int DP, bool kCausal>
@@ -452,12 +656,15 @@ cudaError_t launch_tc(const FwdParams& p, cudaStream_t st) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nq = (p.N + kBM - 1) / kBM;
-  const long long items = static_cast<long long>((nq + kQT - 1) / kQT) * p.B * p.H;
+  const long long items = static_cast<long long>((nq + 1) / 2) * p.B * p.H;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   FwdParams pc = p;
   void* args[] = {&mq, &mk, &mv, &pc};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(static_cast<unsigned>(items)),
-                          dim3(kThreads), args, Cfg::kSmemBytes, st);
+  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads), args,
+                          Cfg::kSmemBytes, st);
 }
 
 }  // namespace

@@ -149,3 +149,16 @@ def test_bounded_wait_self_test_reports_timeout():
     o, lse = api.forward(q, k, v, causal=True)
     assert api.sync_status() == 0
     compare_fwd(inp, o, lse, True, default_scale(64))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d", [(200, 64), (300, 64), (650, 128)])
+def test_many_items_per_cta(causal, N, d):
+    """Enough (b, h) heads that every persistent CTA walks several work items,
+    including single-tile items (odd tile counts); sampled heads in full."""
+    require_gpu()
+    B, H = 40, 16
+    inp = make(B, H, N, d, "bf16", 8600 + N + int(causal))
+    o, lse, _ = run_fwd(inp, causal=causal)
+    heads = [(0, 0), (B - 1, H - 1), (17, 5), (23, 11), (39, 0)]
+    compare_fwd(inp, o, lse, causal, default_scale(d), heads=heads)
