@@ -23,27 +23,39 @@
 // converted to an fp16 copy in shared memory (an MMA takes one input type).
 // This bounds |Q|, |K| and |dS| by fp16's range (65504) in the backward.
 //
-// Both kernels share one skeleton (template parameter kDkDv):
-//   row tile   : the CTA's 128 rows, resident in shared memory for the whole
-//                kernel.  dQ kernel: Q and dO of 128 queries.  dK/dV kernel: K
-//                and V of 128 keys.
-//   loop block : 64 rows streamed through a TMA ring.  dQ: K_j and V_j of 64
-//                keys.  dK/dV: Q_i and dO_i of 64 queries (plus their L, D).
-//   per block  : S = R1 C1^T and dP = R2 C2^T (tcgen05, M=128, N=64, K=d, bf16,
-//                both operands K-major); one thread per row forms P and dS and
-//                writes them back to TMEM (P in S's columns, dS in dP's); then
+// Both kernels share one persistent skeleton (template parameter kDkDv): one
+// CTA per SM walks work items, each a 128-row tile of one (b, h):
+//   row tile   : resident in shared memory for the item.  dQ kernel: Q and dO
+//                of 128 queries.  dK/dV kernel: K and V of 128 keys.
+//   blocks     : streamed through a TMA ring.  dQ: K_j, V_j.  dK/dV: Q_i, dO_i
+//                (plus their L and D).
+//   per block  : S = R1 C1^T and dP = R2 C2^T (tcgen05, M=128, bf16, both
+//                operands K-major); one thread per row forms P and dS and
+//                writes them to TMEM; then
 //                dQ kernel:    dQ += dS K_j, B += P K_j      (fp16)
 //                dK/dV kernel: dV += P dO_i (bf16), dK += dS Q_i (fp16)
 //                with A read from TMEM and B the streamed tile as an MN-major
 //                operand.
-//   S and dP are double-buffered in TMEM and two element-wise warpgroups take
-//   alternate blocks, so one block's exponentials overlap the other block's
-//   MMAs.
+// Two layouts (TMEM is 512 columns):
+//   head dim <= 64 ("wide"): 128-row blocks, so the S and dP MMAs are
+//     128 x 128; both element-wise warpgroups work on every block (64 columns
+//     each); S and dP are released as soon as they are in registers and P, dS
+//     have their own columns, so the next block's S and dP MMAs run while the
+//     current block's exponentials are computed.
+//     columns: S [0,128) dP [128,256) acc1 [256,320) acc2 [320,384)
+//              P [384,448) dS [448,512)
+//   head dim <= 128 ("narrow"): 64-row blocks; S and dP double-buffered, P and
+//     dS written over them, the two warpgroups take alternate blocks.
+//     columns: S [0,128) dP [128,256) acc1 [256,384) acc2 [384,512)
+// Items are numbered head-major (CTAs working at one time share a few heads'
+// streamed tiles through L2) and odd waves run in reverse CTA order, which
+// pairs long and short causal tiles on each CTA.
 //
-// Roles (12 warps): warp 0 TMA producer, warp 1 MMA issuer, warp 2 loads the
-// per-query L and D of each block (dK/dV kernel), warp 3 converts the streamed
-// C1 tile to fp16, warps 4-7 and 8-11 are the element-wise warpgroups (and the
-// epilogue: each stores half of the columns of the accumulator rows).
+// Roles (12 warps): warp 0 TMA producer, warp 1 MMA issuer (converged, lane 0
+// issues), warp 2 loads the per-query L and D of each block (dK/dV kernel),
+// warp 3 converts each streamed C1 tile to fp16, warps 4-7 and 8-11 are the
+// element-wise warpgroups and the epilogue (each stores half of the columns
+// of the accumulator rows).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -58,23 +70,23 @@
 namespace fa {
 namespace {
 
-constexpr int kRows = 128;       // rows owned by a CTA
-constexpr int kBlk = 64;         // rows of one streamed block
+constexpr int kRows = 128;       // rows owned by a work item
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
-constexpr int kMaxStages = 4;
+constexpr int kStagesMax = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int DP>
 struct BwdCfg {
-  static constexpr int kStages = (DP == 64) ? 4 : 3;
+  static constexpr bool kWide = (DP == 64);
+  static constexpr int kBlk = kWide ? 128 : 64;          // rows of one streamed block
+  static constexpr int kStages = 3;
   static constexpr int kChunks = DP / 64;
   static constexpr int kRowChunk = kRows * 128;          // 16 KB: 128 rows x 64 cols
-  static constexpr int kBlkChunk = kBlk * 128;           // 8 KB: 64 rows x 64 cols
+  static constexpr int kBlkChunk = kBlk * 128;           // rows x 64 cols
   static constexpr int kRowTile = kChunks * kRowChunk;
   static constexpr int kBlkTile = kChunks * kBlkChunk;
-  static constexpr int kVecBytes = 1024;                 // L2 and D of 64 queries (512 B),
-                                                         // padded to keep stages 1 KB aligned
+  static constexpr int kVecBytes = 1024;                 // L2 and D of up to 128 queries
   // stage: C1 (bf16) | C2 (bf16) | C1 as fp16 | vectors
   static constexpr int kStageBytes = 3 * kBlkTile + kVecBytes;
   static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
@@ -82,27 +94,26 @@ struct BwdCfg {
   static constexpr int kR2Off = kRowTile;
   static constexpr int kStageOff = 2 * kRowTile;
   static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kDsumOff = kBarOff + 512;         // 2 x 128 floats
-  static constexpr int kSmemBytes = kDsumOff + 1024 + 1024;
+  static constexpr int kDsumOff = kBarOff + 512;         // 2 items x 2 warpgroups x 128
+  static constexpr int kSmemBytes = kDsumOff + 2048 + 1024;
   // TMEM columns
-  static constexpr int kTS = 0;            // S buffers: kTS + b * 64 (P written over S)
-  static constexpr int kTdP = 128;         // dP buffers: kTdP + b * 64 (dS written over dP)
-  static constexpr int kTAcc1 = 256;       // dV (dK/dV kernel) or B (dQ kernel)
-  static constexpr int kTAcc2 = 256 + DP;  // dK or dQ
+  static constexpr int kTS = 0;
+  static constexpr int kTdP = 128;
+  static constexpr int kTAcc1 = 256;                     // dV, or B (dQ kernel)
+  static constexpr int kTAcc2 = 256 + DP;                // dK or dQ
+  static constexpr int kTP = 384;                        // wide layout only
+  static constexpr int kTdS = 448;                       // wide layout only
+  static_assert(kWide || DP == 128, "head dims pad to 64 or 128");
 };
 
 struct BwdBars {
-  uint64_t r_full;
-  uint64_t c_full[kMaxStages];
-  uint64_t c_empty[kMaxStages];
-  uint64_t vec_full[kMaxStages];
-  uint64_t conv_full[kMaxStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t acc_full;
-  uint64_t dsum;
-  uint64_t drain;
-  uint64_t probe;
+  uint64_t r_full, r_empty;
+  uint64_t c_full[kStagesMax], c_empty[kStagesMax];
+  uint64_t vec_full[kStagesMax], conv_full[kStagesMax];
+  uint64_t sp_full, sp_free, pd_full, acc_done;   // wide layout
+  uint64_t s_full[2], p_full[2];                  // narrow layout
+  uint64_t acc_full, acc_free, dsum;
+  uint64_t drain, probe;
   uint32_t tmem_base;
   int abort;
 };
@@ -118,6 +129,44 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, budget));
 }
 
+// Static schedule: the li-th item of this CTA (see the header); -1 when done.
+__device__ __forceinline__ int item_index(int li, int num_items) {
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long base = static_cast<long long>(li) * G;
+  if (base >= num_items) return -1;
+  const bool reverse = (li & 1) && base + G <= num_items;
+  const long long it = base + (reverse ? G - 1 - c : c);
+  return it < num_items ? static_cast<int>(it) : -1;
+}
+
+struct Item {
+  int b, h, row0, i0, nb;   // streamed blocks [i0, i0 + nb)
+};
+
+template <bool kDkDv, bool kCausal, int kBlk>
+__device__ __forceinline__ Item decode_item(int it, int N, int H) {
+  const int ntiles = (N + kRows - 1) / kRows;
+  const int nblocks = (N + kBlk - 1) / kBlk;
+  const int bh = it / ntiles, traw = it % ntiles;
+  // within a head the longest tile first: dK/dV tiles near the start see the
+  // most queries (causal), dQ tiles near the end see the most keys
+  const int tile = kDkDv ? traw : (ntiles - 1 - traw);
+  Item w;
+  w.b = bh / H;
+  w.h = bh % H;
+  w.row0 = tile * kRows;
+  int i1;
+  if (kDkDv) {
+    w.i0 = kCausal ? (w.row0 / kBlk) : 0;
+    i1 = nblocks;
+  } else {
+    w.i0 = 0;
+    i1 = kCausal ? min(nblocks, (w.row0 + kRows + kBlk - 1) / kBlk) : nblocks;
+  }
+  w.nb = i1 - w.i0;
+  return w;
+}
+
 // Store 32-column groups [col0, col0 + ncols) of this thread's accumulator row
 // at TMEM address `acc`, as mult * (acc + corr * acc_b) (acc_b read only when
 // kCorr), to a row of d elements of type float or bf16.
@@ -127,6 +176,7 @@ __device__ __forceinline__ void store_acc_cols(uint32_t acc, uint32_t acc_b, flo
                                                bool store) {
   for (int cc = col0; cc < col0 + ncols; cc += 32) {
     uint32_t r[32];
+    __syncwarp();   // the stores below are per-thread; tcgen05.ld is collective
     tmem_ld32(acc + cc, r);
     tmem_ld_wait(r);
     if (kCorr) {
@@ -186,7 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmC2,
                   const BwdParams p) {
   using Cfg = BwdCfg<DP>;
-  constexpr int kStages = Cfg::kStages;
+  constexpr int S = Cfg::kStages;
+  constexpr int kBlk = Cfg::kBlk;
+  constexpr bool kWide = Cfg::kWide;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -194,42 +246,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* dsum = reinterpret_cast<float*>(smem + Cfg::kDsumOff);
   const volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-
-  // ---- work item ----
   const int N = p.N, H = p.H;
-  const int ntiles = (N + kRows - 1) / kRows;
-  const int nblocks = (N + kBlk - 1) / kBlk;
-  const int item = blockIdx.x;
-  // Head-major order (the CTAs of one head share its streamed tiles through
-  // L2); within a head the longest tile first: dK/dV tiles near the start see
-  // the most queries (causal), dQ tiles near the end see the most keys.
-  const int tile = kDkDv ? (item % ntiles) : (ntiles - 1 - item % ntiles);
-  const int bh = item / ntiles, b = bh / H, h = bh % H;
-  const int row0 = tile * kRows;
-  int i0, i1;  // streamed blocks [i0, i1)
-  if (kDkDv) {
-    i0 = kCausal ? (row0 / kBlk) : 0;
-    i1 = nblocks;
-  } else {
-    i0 = 0;
-    i1 = kCausal ? min(nblocks, (row0 + kRows) / kBlk) : nblocks;
-  }
-  const int nb = i1 - i0;
+  const int num_items = ((N + kRows - 1) / kRows) * p.B * H;
 
   // ---- setup ----
   if (threadIdx.x == 0) {
     mbar_init(&bars->r_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    mbar_init(&bars->r_empty, 1);
+    for (int s = 0; s < S; ++s) {
       mbar_init(&bars->c_full[s], 1);
       mbar_init(&bars->c_empty[s], 1);
       mbar_init(&bars->vec_full[s], 32);
       mbar_init(&bars->conv_full[s], 32);
     }
+    mbar_init(&bars->sp_full, 1);
+    mbar_init(&bars->sp_free, 256);
+    mbar_init(&bars->pd_full, 256);
+    mbar_init(&bars->acc_done, 1);
     for (int g = 0; g < 2; ++g) {
       mbar_init(&bars->s_full[g], 1);
       mbar_init(&bars->p_full[g], 128);
     }
     mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_free, 256);
     mbar_init(&bars->dsum, 256);
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->probe, 1);
@@ -269,225 +308,313 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmR2);
       tma_prefetch_desc(&tmC1);
       tma_prefetch_desc(&tmC2);
-      mbar_arrive_expect_tx(&bars->r_full, 2 * Cfg::kRowTile);
-      for (int c = 0; c < Cfg::kChunks; ++c) {
-        tma_load_4d(sR1 + c * Cfg::kRowChunk, &tmR1, &bars->r_full, c * 64, h, row0, b);
-        tma_load_4d(sR2 + c * Cfg::kRowChunk, &tmR2, &bars->r_full, c * 64, h, row0, b);
-      }
-      int issued = 0;
-      for (int t = 0; t < nb; ++t) {
-        const int s = t % kStages, round = t / kStages;
-        if (round > 0 &&
-            !mbar_wait(&bars->c_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
-          raise_abort(bars, p.status);
+      int c = 0, li = 0;
+      bool ok = true;
+      for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(li, num_items)) {
+        const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
+        if (li > 0 && !mbar_wait(&bars->r_empty, (li - 1) & 1, abort_flag, kWaitBudget)) {
+          ok = false;
           break;
         }
-        const int r = (i0 + t) * kBlk;
-        mbar_arrive_expect_tx(&bars->c_full[s], 2 * Cfg::kBlkTile);
-        for (int c = 0; c < Cfg::kChunks; ++c) {
-          tma_load_4d(stage_c1(s) + c * Cfg::kBlkChunk, &tmC1, &bars->c_full[s], c * 64, h, r, b);
-          tma_load_4d(stage_c2(s) + c * Cfg::kBlkChunk, &tmC2, &bars->c_full[s], c * 64, h, r, b);
+        mbar_arrive_expect_tx(&bars->r_full, 2 * Cfg::kRowTile);
+        for (int ch = 0; ch < Cfg::kChunks; ++ch) {
+          tma_load_4d(sR1 + ch * Cfg::kRowChunk, &tmR1, &bars->r_full, ch * 64, w.h, w.row0, w.b);
+          tma_load_4d(sR2 + ch * Cfg::kRowChunk, &tmR2, &bars->r_full, ch * 64, w.h, w.row0, w.b);
         }
-        issued = t + 1;
+        ++li;
+        for (int t = 0; t < w.nb; ++t) {
+          const int s = c % S, round = c / S;
+          if (round > 0 &&
+              !mbar_wait(&bars->c_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
+          }
+          const int r = (w.i0 + t) * kBlk;
+          mbar_arrive_expect_tx(&bars->c_full[s], 2 * Cfg::kBlkTile);
+          for (int ch = 0; ch < Cfg::kChunks; ++ch) {
+            tma_load_4d(stage_c1(s) + ch * Cfg::kBlkChunk, &tmC1, &bars->c_full[s], ch * 64, w.h,
+                        r, w.b);
+            tma_load_4d(stage_c2(s) + ch * Cfg::kBlkChunk, &tmC2, &bars->c_full[s], ch * 64, w.h,
+                        r, w.b);
+          }
+          ++c;
+        }
       }
-      for (int t = max(0, issued - kStages); t < issued; ++t)
-        mbar_wait(&bars->c_full[t % kStages], (t / kStages) & 1, nullptr, kDrainBudget);
-      mbar_wait(&bars->r_full, 0, nullptr, kDrainBudget);
+      if (!ok) raise_abort(bars, p.status);
+      for (int x = max(0, c - S); x < c; ++x)
+        mbar_wait(&bars->c_full[x % S], (x / S) & 1, nullptr, kDrainBudget);
+      if (li > 0) mbar_wait(&bars->r_full, (li - 1) & 1, nullptr, kDrainBudget);
     }
     __syncwarp();
   } else if (run && warp == 1) {
     // ============ MMA issuer (whole warp converged, lane 0 issues) ============
-    {
-      const uint32_t leader = (lane == 0) ? 1u : 0u;
-      constexpr uint32_t kIdescSP = idesc_bf16(kRows, kBlk, false, false);
-      constexpr uint32_t kIdescAccBf = idesc_bf16(kRows, DP, false, true);
-      constexpr uint32_t kIdescAccH = idesc_f16(kRows, DP, false, true);
-      const int nks = (p.d + 15) / 16;
-      // descriptor bases; offsets advance the 16-byte start-address field
-      const uint64_t dR1 = sdesc_sw128(smem_u32(sR1), 16, 1024);
-      const uint64_t dR2 = sdesc_sw128(smem_u32(sR2), 16, 1024);
-      const uint64_t dC1 = sdesc_sw128(smem_u32(stage_c1(0)), 16, 1024);
-      const uint64_t dC2 = sdesc_sw128(smem_u32(stage_c2(0)), 16, 1024);
-      const uint64_t dC1hMN = sdesc_sw128(smem_u32(stage_c1h(0)), Cfg::kBlkChunk, 1024);
-      const uint64_t dC2MN = sdesc_sw128(smem_u32(stage_c2(0)), Cfg::kBlkChunk, 1024);
-      bool ok = warp_wait(&bars->r_full, 0, abort_flag, kWaitBudget);
+    const uint32_t leader = (lane == 0) ? 1u : 0u;
+    constexpr uint32_t kIdescSP = idesc_bf16(kRows, kBlk, false, false);
+    constexpr uint32_t kIdescAccBf = idesc_bf16(kRows, DP, false, true);
+    constexpr uint32_t kIdescAccH = idesc_f16(kRows, DP, false, true);
+    const int nks = (p.d + 15) / 16;
+    // descriptor bases; offsets advance the 16-byte start-address field
+    const uint64_t dR1 = sdesc_sw128(smem_u32(sR1), 16, 1024);
+    const uint64_t dR2 = sdesc_sw128(smem_u32(sR2), 16, 1024);
+    const uint64_t dC1 = sdesc_sw128(smem_u32(stage_c1(0)), 16, 1024);
+    const uint64_t dC2 = sdesc_sw128(smem_u32(stage_c2(0)), 16, 1024);
+    const uint64_t dC1hMN = sdesc_sw128(smem_u32(stage_c1h(0)), Cfg::kBlkChunk, 1024);
+    const uint64_t dC2MN = sdesc_sw128(smem_u32(stage_c2(0)), Cfg::kBlkChunk, 1024);
 
-      auto issue_sp = [&](int t) {
-        const int s = t % kStages, buf = t & 1;
-        const uint64_t so = static_cast<uint64_t>((s * Cfg::kStageBytes) >> 4);
-        for (int kk = 0; kk < nks; ++kk) {
-          const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * Cfg::kRowChunk + (kk & 3) * 32) >> 4);
-          const uint64_t co = static_cast<uint64_t>(((kk >> 2) * Cfg::kBlkChunk + (kk & 3) * 32) >> 4);
-          mma_ss_w(tmem + Cfg::kTS + buf * kBlk, dR1 + ro, dC1 + so + co, kIdescSP, kk > 0, leader);
-          mma_ss_w(tmem + Cfg::kTdP + buf * kBlk, dR2 + ro, dC2 + so + co, kIdescSP, kk > 0,
-                   leader);
-        }
-        mma_commit_w(&bars->s_full[buf], leader);
-      };
-      auto issue_acc = [&](int t) {
-        const int s = t % kStages, buf = t & 1;
-        const uint64_t so = static_cast<uint64_t>((s * Cfg::kStageBytes) >> 4);
+    // S and dP of global block cb into TMEM column offset `col`
+    auto issue_sp = [&](int cb, int col) {
+      const uint64_t so = static_cast<uint64_t>(((cb % S) * Cfg::kStageBytes) >> 4);
+      for (int kk = 0; kk < nks; ++kk) {
+        const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * Cfg::kRowChunk + (kk & 3) * 32) >> 4);
+        const uint64_t co = static_cast<uint64_t>(((kk >> 2) * Cfg::kBlkChunk + (kk & 3) * 32) >> 4);
+        mma_ss_w(tmem + Cfg::kTS + col, dR1 + ro, dC1 + so + co, kIdescSP, kk > 0, leader);
+        mma_ss_w(tmem + Cfg::kTdP + col, dR2 + ro, dC2 + so + co, kIdescSP, kk > 0, leader);
+      }
+    };
+    // accumulating MMAs of global block cb; P and dS at TMEM columns pcol, dcol
+    auto issue_acc = [&](int cb, bool first, uint32_t pcol, uint32_t dcol) {
+      const uint64_t so = static_cast<uint64_t>(((cb % S) * Cfg::kStageBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk) {
-          const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t pa = tmem + Cfg::kTS + buf * kBlk + kk * 8;    // P
-          const uint32_t da = tmem + Cfg::kTdP + buf * kBlk + kk * 8;   // dS
-          const uint64_t ko = static_cast<uint64_t>((kk * 2048) >> 4);
-          if (kDkDv)  // dV += P dO_i (bf16)
-            mma_ts_w(tmem + Cfg::kTAcc1, pa, dC2MN + so + ko, kIdescAccBf, acc, leader);
-          else        // B += P K_j (fp16)
-            mma_ts_w(tmem + Cfg::kTAcc1, pa, dC1hMN + so + ko, kIdescAccH, acc, leader);
-          // dK += dS Q_i   or   dQ += dS K_j   (fp16)
-          mma_ts_w(tmem + Cfg::kTAcc2, da, dC1hMN + so + ko, kIdescAccH, acc, leader);
-        }
-        mma_commit_w(&bars->c_empty[s], leader);
-      };
-      auto ready_acc = [&](int t) {
-        return warp_wait(&bars->p_full[t & 1], (t >> 1) & 1, abort_flag, kWaitBudget) &&
-               warp_wait(&bars->conv_full[t % kStages], (t / kStages) & 1, abort_flag,
-                         kWaitBudget);
-      };
+      for (int kk = 0; kk < kBlk / 16; ++kk) {
+        const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+        const uint32_t pa = tmem + pcol + kk * 8;
+        const uint32_t da = tmem + dcol + kk * 8;
+        const uint64_t ko = static_cast<uint64_t>((kk * 2048) >> 4);
+        if (kDkDv)  // dV += P dO_i (bf16)
+          mma_ts_w(tmem + Cfg::kTAcc1, pa, dC2MN + so + ko, kIdescAccBf, acc, leader);
+        else        // B += P K_j (fp16)
+          mma_ts_w(tmem + Cfg::kTAcc1, pa, dC1hMN + so + ko, kIdescAccH, acc, leader);
+        // dK += dS Q_i   or   dQ += dS K_j   (fp16)
+        mma_ts_w(tmem + Cfg::kTAcc2, da, dC1hMN + so + ko, kIdescAccH, acc, leader);
+      }
+      mma_commit_w(&bars->c_empty[cb % S], leader);
+    };
+    auto wait_c = [&](int cb) {
+      return warp_wait(&bars->c_full[cb % S], (cb / S) & 1, abort_flag, kWaitBudget);
+    };
+    auto wait_acc_inputs = [&](int cb, bool item_first, int li) {
+      bool ok = warp_wait(&bars->conv_full[cb % S], (cb / S) & 1, abort_flag, kWaitBudget);
+      // the first accumulation of an item overwrites the accumulators: the
+      // previous item's epilogue must have read them
+      if (ok && item_first && li > 0)
+        ok = warp_wait(&bars->acc_free, (li - 1) & 1, abort_flag, kWaitBudget);
+      return ok;
+    };
 
-      for (int t = 0; t < nb && ok; ++t) {
-        if (!warp_wait(&bars->c_full[t % kStages], (t / kStages) & 1, abort_flag, kWaitBudget)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_sp(t);
-        if (t >= 1) {
-          if (!ready_acc(t - 1)) {
+    int c = 0, li = 0;
+    int nsp = 0;   // wide: S/dP groups issued; narrow: unused
+    int npd = 0;   // wide: pd_full phases consumed
+    bool ok = true;
+    for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
+      const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
+      if (!warp_wait(&bars->r_full, li & 1, abort_flag, kWaitBudget)) {
+        ok = false;
+        break;
+      }
+      if constexpr (kWide) {
+        auto next_sp = [&](int cb) -> bool {
+          if (!wait_c(cb)) return false;
+          if (nsp > 0 && !warp_wait(&bars->sp_free, (nsp - 1) & 1, abort_flag, kWaitBudget))
+            return false;
+          tc_fence_after();
+          issue_sp(cb, 0);
+          mma_commit_w(&bars->sp_full, leader);
+          ++nsp;
+          return true;
+        };
+        if (!next_sp(c)) { ok = false; break; }
+        for (int t = 0; t < w.nb; ++t) {
+          const int cb = c + t;
+          if (t + 1 < w.nb) {
+            if (!next_sp(cb + 1)) { ok = false; break; }
+          } else {
+            mma_commit_w(&bars->r_empty, leader);   // all S/dP of this item issued
+          }
+          if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
+              !wait_acc_inputs(cb, t == 0, li)) {
             ok = false;
             break;
           }
+          ++npd;
           tc_fence_after();
-          issue_acc(t - 1);
+          issue_acc(cb, t == 0, Cfg::kTP, Cfg::kTdS);
+          mma_commit_w(&bars->acc_done, leader);
+          if (t == w.nb - 1) mma_commit_w(&bars->acc_full, leader);
+        }
+      } else {
+        // narrow: S/dP of global block cb go to buffer cb & 1; warpgroup cb & 1
+        // forms P and dS in place
+        for (int t = 0; t <= w.nb && ok; ++t) {
+          const int cb = c + t;
+          if (t < w.nb) {
+            if (!wait_c(cb)) { ok = false; break; }
+            tc_fence_after();
+            issue_sp(cb, (cb & 1) * kBlk);
+            mma_commit_w(&bars->s_full[cb & 1], leader);
+            if (t == w.nb - 1) mma_commit_w(&bars->r_empty, leader);
+          }
+          if (t >= 1) {
+            const int pb = cb - 1;
+            if (!warp_wait(&bars->p_full[pb & 1], (pb >> 1) & 1, abort_flag, kWaitBudget) ||
+                !wait_acc_inputs(pb, t == 1, li)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_acc(pb, t == 1, Cfg::kTS + (pb & 1) * kBlk, Cfg::kTdP + (pb & 1) * kBlk);
+            if (t == w.nb) mma_commit_w(&bars->acc_full, leader);
+          }
         }
       }
-      if (ok) {
-        if (ready_acc(nb - 1)) {
-          tc_fence_after();
-          issue_acc(nb - 1);
-          mma_commit_w(&bars->acc_full, leader);
-        } else {
-          ok = false;
-        }
-      }
-      if (!ok && leader) raise_abort(bars, p.status);
-      mma_commit_w(&bars->drain, leader);
-      mbar_wait(&bars->drain, 0, nullptr, kDrainBudget);
+      c += w.nb;
     }
+    if (!ok && leader) raise_abort(bars, p.status);
+    mma_commit_w(&bars->drain, leader);
+    mbar_wait(&bars->drain, 0, nullptr, kDrainBudget);
     __syncwarp();
   } else if (run && warp == 2) {
     // ============ per-query L and D of each streamed block (dK/dV) ============
     if (kDkDv) {
-      const float* lse = p.lse + static_cast<size_t>(bh) * N;
-      const float* Dv = p.D + static_cast<size_t>(bh) * N;
-      for (int t = 0; t < nb; ++t) {
-        const int s = t % kStages, round = t / kStages;
-        if (round > 0 &&
-            !warp_wait(&bars->c_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
-          if (lane == 0) raise_abort(bars, p.status);
-          break;
-        }
-        float* vec = stage_vec(s);
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = u * 32 + lane;
-          const int q = (i0 + t) * kBlk + c;
-          float l2 = INFINITY, dd = 0.0f;   // padded or fully masked query: P = 0
-          if (q < N) {
-            const float L = lse[q];
-            if (L != -INFINITY) {
-              l2 = L * kLog2e;
-              dd = Dv[q];
-            }
+      int c = 0, li = 0;
+      bool ok = true;
+      for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
+        const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
+        const size_t hb = (static_cast<size_t>(w.b) * H + w.h) * N;
+        for (int t = 0; t < w.nb; ++t, ++c) {
+          const int s = c % S, round = c / S;
+          if (round > 0 &&
+              !warp_wait(&bars->c_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
           }
-          vec[c] = l2;
-          vec[kBlk + c] = dd;
+          float* vec = stage_vec(s);
+#pragma unroll
+          for (int u = 0; u < kBlk / 32; ++u) {
+            const int col = u * 32 + lane;
+            const int q = (w.i0 + t) * kBlk + col;
+            float l2 = INFINITY, dd = 0.0f;   // padded or fully masked query: P = 0
+            if (q < N) {
+              const float L = p.lse[hb + q];
+              if (L != -INFINITY) {
+                l2 = L * kLog2e;
+                dd = p.D[hb + q];
+              }
+            }
+            vec[col] = l2;
+            vec[kBlk + col] = dd;
+          }
+          mbar_arrive(&bars->vec_full[s]);
         }
-        mbar_arrive(&bars->vec_full[s]);
       }
+      if (!ok && lane == 0) raise_abort(bars, p.status);
     }
     __syncwarp();
   } else if (run && warp == 3) {
     // ============ fp16 copy of each streamed C1 tile (same swizzled layout) ============
     constexpr int kVecs = Cfg::kBlkTile / 16;
-    for (int t = 0; t < nb; ++t) {
-      const int s = t % kStages;
-      if (!warp_wait(&bars->c_full[s], (t / kStages) & 1, abort_flag, kWaitBudget)) {
-        if (lane == 0) raise_abort(bars, p.status);
-        break;
-      }
-      const uint4* src = reinterpret_cast<const uint4*>(stage_c1(s));
-      uint4* dst = reinterpret_cast<uint4*>(stage_c1h(s));
+    int c = 0, li = 0;
+    bool ok = true;
+    for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
+      const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
+      for (int t = 0; t < w.nb; ++t, ++c) {
+        const int s = c % S;
+        if (!warp_wait(&bars->c_full[s], (c / S) & 1, abort_flag, kWaitBudget)) {
+          ok = false;
+          break;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(stage_c1(s));
+        uint4* dst = reinterpret_cast<uint4*>(stage_c1h(s));
 #pragma unroll 4
-      for (int i = lane; i < kVecs; i += 32) {
-        uint4 v = src[i];
-        v.x = bf16x2_to_f16x2(v.x);
-        v.y = bf16x2_to_f16x2(v.y);
-        v.z = bf16x2_to_f16x2(v.z);
-        v.w = bf16x2_to_f16x2(v.w);
-        dst[i] = v;
+        for (int i = lane; i < kVecs; i += 32) {
+          uint4 v = src[i];
+          v.x = bf16x2_to_f16x2(v.x);
+          v.y = bf16x2_to_f16x2(v.y);
+          v.z = bf16x2_to_f16x2(v.z);
+          v.w = bf16x2_to_f16x2(v.w);
+          dst[i] = v;
+        }
+        fence_proxy_async_smem();   // make the copy visible to the tensor cores
+        mbar_arrive(&bars->conv_full[s]);
       }
-      fence_proxy_async_smem();   // make the copy visible to the tensor cores
-      mbar_arrive(&bars->conv_full[s]);
     }
+    if (!ok && lane == 0) raise_abort(bars, p.status);
     __syncwarp();
   } else if (run && warp >= 4) {
     // ======================= element-wise warpgroups =======================
     const int g = (warp - 4) / 4;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int grow = row0 + row;                    // query (dQ) or key (dK/dV)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_base + Cfg::kTS + g * kBlk;
-    const uint32_t tdP = tmem + lane_base + Cfg::kTdP + g * kBlk;
     const float c = p.scale_log2;
-    float l2_row = INFINITY, d_row = 0.0f;          // dQ kernel: this query's L, D~
-    bool live_row = false;
-    if (!kDkDv && grow < N) {
-      const float L = p.lse[static_cast<size_t>(bh) * N + grow];
-      if (L != -INFINITY) {
-        live_row = true;
-        l2_row = L * kLog2e;
-        d_row = p.D[static_cast<size_t>(bh) * N + grow];
-      }
-    }
-    float d_acc = 0.0f;                             // dQ kernel: sum_j P_ij dP_ij
+    // wide: this warpgroup's 64 columns of every block; narrow: buffer g
+    const uint32_t tS = tmem + lane_base + Cfg::kTS + g * 64;
+    const uint32_t tdP = tmem + lane_base + Cfg::kTdP + g * 64;
+    const uint32_t tP = tmem + lane_base + (kWide ? Cfg::kTP + g * 32 : Cfg::kTS + g * 64);
+    const uint32_t tdS = tmem + lane_base + (kWide ? Cfg::kTdS + g * 32 : Cfg::kTdP + g * 64);
+    const int colg = kWide ? g * 64 : 0;    // first block column this warpgroup handles
+    int cbase = 0, li = 0;
+    int nsp = 0;    // wide: sp_full phases consumed
     bool ok = true;
-    for (int t = g; t < nb; t += 2) {
-      if (!warp_wait(&bars->s_full[g], (t >> 1) & 1, abort_flag, kWaitBudget)) {
-        ok = false;
-        break;
+    for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
+      const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
+      const int grow = w.row0 + row;      // query (dQ) or key (dK/dV)
+      const size_t hb = (static_cast<size_t>(w.b) * H + w.h) * N;
+      float l2_row = INFINITY, d_row = 0.0f;          // dQ kernel: this query's L, D~
+      bool live_row = false;
+      if (!kDkDv && grow < N) {
+        const float L = p.lse[hb + grow];
+        if (L != -INFINITY) {
+          live_row = true;
+          l2_row = L * kLog2e;
+          d_row = p.D[hb + grow];
+        }
       }
-      const int s = t % kStages;
-      if (kDkDv && !warp_wait(&bars->vec_full[s], (t / kStages) & 1, abort_flag, kWaitBudget)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int col0 = (i0 + t) * kBlk;             // first key (dQ) or query (dK/dV)
-      bool masked;
-      if (kDkDv) masked = kCausal && (col0 < row0 + kRows - 1);
-      else masked = (kCausal && (col0 + kBlk - 1 > row0)) || (col0 + kBlk > N);
-      const float* vec = kDkDv ? stage_vec(s) : nullptr;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tS + half * 32, sr);
-        tmem_ld32(tdP + half * 32, dr);
+      float d_acc = 0.0f;                             // dQ kernel: sum_j P_ij dP_ij
+      for (int t = 0; t < w.nb; ++t) {
+        const int cb = cbase + t;
+        if (!kWide && (cb & 1) != g) continue;
+        if (kWide) {
+          if (!warp_wait(&bars->sp_full, nsp & 1, abort_flag, kWaitBudget)) { ok = false; break; }
+          ++nsp;
+        } else {
+          if (!warp_wait(&bars->s_full[g], (cb >> 1) & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
+          }
+        }
+        const int s = cb % S;
+        if (kDkDv &&
+            !warp_wait(&bars->vec_full[s], (cb / S) & 1, abort_flag, kWaitBudget)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[64], dr[64];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld32(tdP, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+        tmem_ld32(tdP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
-        uint32_t pk[16], dk[16];
+        if (kWide) {
+          // S and dP are in registers: the next block's MMAs may overwrite them
+          tc_fence_before();
+          mbar_arrive(&bars->sp_free);
+        }
+        const int col0 = (w.i0 + t) * kBlk + colg;   // first query (dK/dV) or key (dQ)
+        bool masked;
+        if (kDkDv) masked = kCausal && (col0 < w.row0 + kRows - 1);
+        else masked = (kCausal && (col0 + 63 > w.row0)) || (col0 + 64 > N);
+        const float* vec = kDkDv ? stage_vec(s) + colg : nullptr;
+        uint32_t pk[32], dk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 32; ++i) {
           float pp[2], ds[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int cl = half * 32 + 2 * i + e;    // column within the block
-            const float sv = __uint_as_float(sr[2 * i + e]);
-            const float dpv = __uint_as_float(dr[2 * i + e]);
+            const int cl = 2 * i + e;                // column within this warpgroup's 64
+            const float sv = __uint_as_float(sr[cl]);
+            const float dpv = __uint_as_float(dr[cl]);
             float l2, dd;
             if (kDkDv) {
               l2 = vec[cl];
@@ -499,8 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float pv = fast_exp2(fmaf(sv, c, -l2));
             if (masked) {
               const int other = col0 + cl;
-              const bool bad = kDkDv ? (other < grow)
-                                     : ((kCausal && other > grow) || other >= N);
+              const bool bad = kDkDv ? (other < grow) : ((kCausal && other > grow) || other >= N);
               if (bad) pv = 0.0f;
             }
             if (!kDkDv) d_acc = fmaf(pv, dpv, d_acc);
@@ -510,49 +636,61 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[i] = kDkDv ? pack_bf16x2(pp[0], pp[1]) : pack_f16x2(pp[0], pp[1]);
           dk[i] = pack_f16x2(ds[0], ds[1]);
         }
-        tmem_st16(tS + half * 16, pk);
-        tmem_st16(tdP + half * 16, dk);
+        if (kWide) {
+          // P and dS columns are free once the previous block's accumulating
+          // MMAs have completed
+          if (nsp >= 2 &&
+              !warp_wait(&bars->acc_done, nsp & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        __syncwarp();   // tcgen05.st is warp-collective
+        tmem_st32(tP, pk);
+        tmem_st32(tdS, dk);
+        tmem_st_wait();
+        tc_fence_before();
+        if (kWide) mbar_arrive(&bars->pd_full);
+        else mbar_arrive(&bars->p_full[g]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[g]);
-    }
+      if (!ok) break;
 
-    // ---- epilogue: this warpgroup stores half of the accumulator columns ----
-    float corr = 0.0f;
-    if (!kDkDv && ok) {
-      // Combine the two warpgroups' partial sums of D_i = sum_j P_ij dP_ij.
-      dsum[g * kRows + row] = d_acc;
-      mbar_arrive(&bars->dsum);
-      if (!warp_wait(&bars->dsum, 0, abort_flag, kWaitBudget)) ok = false;
-      if (ok) {
-        const float d_exact = dsum[row] + dsum[kRows + row];
+      // ---- epilogue: this warpgroup stores half of the accumulator columns ----
+      float corr = 0.0f;
+      if (!kDkDv) {
+        // Combine the two warpgroups' partial sums of D_i = sum_j P_ij dP_ij.
+        float* ds_item = dsum + (li & 1) * 256;
+        ds_item[g * kRows + row] = d_acc;
+        mbar_arrive(&bars->dsum);
+        if (!warp_wait(&bars->dsum, li & 1, abort_flag, kWaitBudget)) { ok = false; break; }
+        const float d_exact = ds_item[row] + ds_item[kRows + row];
         corr = d_row - d_exact;
-        if (g == 0 && live_row) p.D[static_cast<size_t>(bh) * N + grow] = d_exact;
+        if (g == 0 && live_row) p.D[hb + grow] = d_exact;
       }
-    }
-    if (ok && !warp_wait(&bars->acc_full, 0, abort_flag, kWaitBudget)) ok = false;
-    if (ok) {
+      if (!warp_wait(&bars->acc_full, li & 1, abort_flag, kWaitBudget)) { ok = false; break; }
       tc_fence_after();
       const bool store = grow < N;
-      const size_t roff = ((static_cast<size_t>(b) * N + (store ? grow : 0)) * H + h) *
+      const size_t roff = ((static_cast<size_t>(w.b) * N + (store ? grow : 0)) * H + w.h) *
                           static_cast<size_t>(p.d);
       const int half_cols = DP / 2;
       const int cbeg = g * half_cols;
-      const uint32_t tbase = tmem + lane_base;
       auto row_ptr = [&](void* base) -> void* {
         return kF32Grad ? static_cast<void*>(static_cast<float*>(base) + roff)
                         : static_cast<void*>(static_cast<__nv_bfloat16*>(base) + roff);
       };
       if (kDkDv) {
-        store_acc_cols<kF32Grad, false>(tbase + Cfg::kTAcc1, 0, 0.0f, cbeg, half_cols, 1.0f,
-                                        row_ptr(p.dv), p.d, store);
-        store_acc_cols<kF32Grad, false>(tbase + Cfg::kTAcc2, 0, 0.0f, cbeg, half_cols, p.scale,
-                                        row_ptr(p.dk), p.d, store);
+        store_acc_cols<kF32Grad, false>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg, half_cols,
+                                        1.0f, row_ptr(p.dv), p.d, store);
+        store_acc_cols<kF32Grad, false>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg, half_cols,
+                                        p.scale, row_ptr(p.dk), p.d, store);
       } else {
-        store_acc_cols<kF32Grad, true>(tbase + Cfg::kTAcc2, tbase + Cfg::kTAcc1, corr, cbeg,
-                                       half_cols, p.scale, row_ptr(p.dq), p.d, store);
+        store_acc_cols<kF32Grad, true>(tmem + lane_base + Cfg::kTAcc2, tmem + lane_base + Cfg::kTAcc1,
+                                       corr, cbeg, half_cols, p.scale, row_ptr(p.dq), p.d, store);
       }
+      tc_fence_before();
+      mbar_arrive(&bars->acc_free);
+      cbase += w.nb;
     }
     if (!ok) raise_abort(bars, p.status);
     __syncwarp();
@@ -567,11 +705,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
 template <int DP, bool kCausal, bool kDkDv, bool kF32>
 cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
   using Cfg = BwdCfg<DP>;
   CUtensorMap m[4];
-  // dQ:    rows are Q, dO (128-row boxes), blocks are K, V (64-row boxes).
+  // dQ:    rows are Q, dO (128-row boxes), blocks are K, V.
   // dK/dV: rows are K, V, blocks are Q, dO.
   const void* r1 = kDkDv ? p.k : p.q;
   const void* r2 = kDkDv ? p.v : p.dO;
@@ -579,18 +724,21 @@ cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
   const void* c2 = kDkDv ? p.dO : p.v;
   cudaError_t e = make_bhnd_tmap(&m[0], r1, p.B, p.N, p.H, p.d, kRows, 64);
   if (e == cudaSuccess) e = make_bhnd_tmap(&m[1], r2, p.B, p.N, p.H, p.d, kRows, 64);
-  if (e == cudaSuccess) e = make_bhnd_tmap(&m[2], c1, p.B, p.N, p.H, p.d, kBlk, 64);
-  if (e == cudaSuccess) e = make_bhnd_tmap(&m[3], c2, p.B, p.N, p.H, p.d, kBlk, 64);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&m[2], c1, p.B, p.N, p.H, p.d, Cfg::kBlk, 64);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&m[3], c2, p.B, p.N, p.H, p.d, Cfg::kBlk, 64);
   if (e != cudaSuccess) return e;
   auto kern = bwd_tc_kernel<DP, kCausal, kDkDv, kF32>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>((p.N + kRows - 1) / kRows) * p.B * p.H;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   BwdParams pc = p;
   void* args[] = {&m[0], &m[1], &m[2], &m[3], &pc};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(static_cast<unsigned>(items)),
-                          dim3(kThreads), args, Cfg::kSmemBytes, st);
+  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads), args,
+                          Cfg::kSmemBytes, st);
 }
 
 // Phase 1 is the dQ kernel: it refines D in the workspace, which the dK/dV

@@ -515,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < DP / 32; ++cc) {
             uint32_t orr[32];
+            __syncwarp();   // tcgen05.ld/st are warp-collective
             tmem_ld32(tO + cc * 32, orr);
             tmem_ld_wait(orr);
 #pragma unroll
@@ -561,9 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           if (rescale) rescale_o();
+          __syncwarp();
           tmem_st32(tP + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         } else {
+          __syncwarp();
           tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         }
@@ -590,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < DP / 32; ++cc) {
         uint32_t orr[32];
+        __syncwarp();   // the stores below are per-thread; tcgen05.ld is collective
         tmem_ld32(tO + cc * 32, orr);
         tmem_ld_wait(orr);
         if (store) {
