@@ -364,30 +364,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S and dP of global block cb into TMEM column offset `col`
     auto issue_sp = [&](int cb, int col) {
       const uint64_t so = static_cast<uint64_t>(((cb % S) * Cfg::kStageBytes) >> 4);
-      for (int kk = 0; kk < nks; ++kk) {
-        const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * Cfg::kRowChunk + (kk & 3) * 32) >> 4);
-        const uint64_t co = static_cast<uint64_t>(((kk >> 2) * Cfg::kBlkChunk + (kk & 3) * 32) >> 4);
-        mma_ss_w(tmem + Cfg::kTS + col, dR1 + ro, dC1 + so + co, kIdescSP, kk > 0, leader);
-        mma_ss_w(tmem + Cfg::kTdP + col, dR2 + ro, dC2 + so + co, kIdescSP, kk > 0, leader);
+      if (leader) {
+        for (int kk = 0; kk < nks; ++kk) {
+          const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * Cfg::kRowChunk + (kk & 3) * 32) >> 4);
+          const uint64_t co = static_cast<uint64_t>(((kk >> 2) * Cfg::kBlkChunk + (kk & 3) * 32) >> 4);
+          mma_ss(tmem + Cfg::kTS + col, dR1 + ro, dC1 + so + co, kIdescSP, kk > 0);
+          mma_ss(tmem + Cfg::kTdP + col, dR2 + ro, dC2 + so + co, kIdescSP, kk > 0);
+        }
       }
+      __syncwarp();
     };
     // accumulating MMAs of global block cb; P and dS at TMEM columns pcol, dcol
     auto issue_acc = [&](int cb, bool first, uint32_t pcol, uint32_t dcol) {
       const uint64_t so = static_cast<uint64_t>(((cb % S) * Cfg::kStageBytes) >> 4);
+      if (leader) {
 #pragma unroll
-      for (int kk = 0; kk < kBlk / 16; ++kk) {
-        const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-        const uint32_t pa = tmem + pcol + kk * 8;
-        const uint32_t da = tmem + dcol + kk * 8;
-        const uint64_t ko = static_cast<uint64_t>((kk * 2048) >> 4);
-        if (kDkDv)  // dV += P dO_i (bf16)
-          mma_ts_w(tmem + Cfg::kTAcc1, pa, dC2MN + so + ko, kIdescAccBf, acc, leader);
-        else        // B += P K_j (fp16)
-          mma_ts_w(tmem + Cfg::kTAcc1, pa, dC1hMN + so + ko, kIdescAccH, acc, leader);
-        // dK += dS Q_i   or   dQ += dS K_j   (fp16)
-        mma_ts_w(tmem + Cfg::kTAcc2, da, dC1hMN + so + ko, kIdescAccH, acc, leader);
+        for (int kk = 0; kk < kBlk / 16; ++kk) {
+          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+          const uint32_t pa = tmem + pcol + kk * 8;
+          const uint32_t da = tmem + dcol + kk * 8;
+          const uint64_t ko = static_cast<uint64_t>((kk * 2048) >> 4);
+          if (kDkDv)  // dV += P dO_i (bf16)
+            mma_ts(tmem + Cfg::kTAcc1, pa, dC2MN + so + ko, kIdescAccBf, acc);
+          else        // B += P K_j (fp16)
+            mma_ts(tmem + Cfg::kTAcc1, pa, dC1hMN + so + ko, kIdescAccH, acc);
+          // dK += dS Q_i   or   dQ += dS K_j   (fp16)
+          mma_ts(tmem + Cfg::kTAcc2, da, dC1hMN + so + ko, kIdescAccH, acc);
+        }
+        mma_commit(&bars->c_empty[cb % S]);
       }
-      mma_commit_w(&bars->c_empty[cb % S], leader);
+      __syncwarp();
     };
     auto wait_c = [&](int cb) {
       return warp_wait(&bars->c_full[cb % S], (cb / S) & 1, abort_flag, kWaitBudget);

@@ -87,8 +87,8 @@ struct FwdCfg {
 };
 
 struct FwdBars {
-  uint64_t q_full;
-  uint64_t q_empty;
+  uint64_t q_full[kQT];    // separate-P layout: per tile; aliased layout: [0] for both
+  uint64_t q_empty[kQT];
   uint64_t k_full[4];
   uint64_t v_full[4];
   uint64_t kv_empty[4];
@@ -176,10 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- setup: barriers, TMEM ----
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
 #pragma unroll
     for (int g = 0; g < kQT; ++g) {
+      mbar_init(&bars->q_full[g], 1);
+      mbar_init(&bars->q_empty[g], 1);
       mbar_init(&bars->s_full[g], 1);
       mbar_init(&bars->s_free[g], kBM);
       mbar_init(&bars->p_full[g], kBM);
@@ -189,9 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kv_empty[s], Cfg::kSepP ? kQT : 1);   // one commit per MMA warp
     }
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, Cfg::kSepP ? kQT : 1);   // one commit per MMA warp
     mbar_init(&bars->probe, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -226,21 +226,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      int c = 0;        // K/V blocks issued so far
-      int li = 0;       // items started by this CTA
+      int c = 0;             // K/V blocks issued so far
+      int li = 0;            // items started by this CTA
+      int qn[kQT] = {0, 0};  // Q loads per tile slot (separate-P layout)
       bool ok = true;
       for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(li, num_items)) {
         const Item w = decode_item<kCausal>(it, nq, nk, H);
-        if (li > 0 && !mbar_wait(&bars->q_empty, (li - 1) & 1, abort_flag, kWaitBudget)) {
-          ok = false;
-          break;
+        if constexpr (Cfg::kSepP) {
+          // each tile slot's Q is reloaded once its previous scores are done
+          for (int g = 0; g < kQT && ok; ++g) {
+            if (w.tile[g] < 0) continue;
+            if (qn[g] > 0 &&
+                !mbar_wait(&bars->q_empty[g], (qn[g] - 1) & 1, abort_flag, kWaitBudget)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars->q_full[g], Cfg::kTileBytes);
+            for (int ch = 0; ch < Cfg::kChunks; ++ch)
+              tma_load_4d(sQ + g * Cfg::kTileBytes + ch * kChunkBytes, &tmQ, &bars->q_full[g],
+                          ch * 64, w.h, w.tile[g] * kBM, w.b);
+            ++qn[g];
+          }
+          if (!ok) break;
+        } else {
+          if (li > 0 && !mbar_wait(&bars->q_empty[0], (li - 1) & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
+          }
+          const int nact = (w.tile[1] < 0) ? 1 : 2;
+          mbar_arrive_expect_tx(&bars->q_full[0], nact * Cfg::kTileBytes);
+          for (int g = 0; g < nact; ++g)
+            for (int ch = 0; ch < Cfg::kChunks; ++ch)
+              tma_load_4d(sQ + g * Cfg::kTileBytes + ch * kChunkBytes, &tmQ, &bars->q_full[0],
+                          ch * 64, w.h, w.tile[g] * kBM, w.b);
         }
-        const int nact = (w.tile[1] < 0) ? 1 : 2;
-        mbar_arrive_expect_tx(&bars->q_full, nact * Cfg::kTileBytes);
-        for (int g = 0; g < nact; ++g)
-          for (int ch = 0; ch < Cfg::kChunks; ++ch)
-            tma_load_4d(sQ + g * Cfg::kTileBytes + ch * kChunkBytes, &tmQ, &bars->q_full, ch * 64,
-                        w.h, w.tile[g] * kBM, w.b);
         ++li;
         for (int j = 0; j < w.nmax; ++j) {
           const int s = c % S, round = c / S;
@@ -262,16 +281,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) raise_abort(bars, p.status);
       // Drain: every issued copy has landed before the CTA may exit.  c counts
-      // the K/V blocks issued; li the Q loads (phase li-1 of q_full is last).
+      // the K/V blocks issued; the last Q load of each slot is its last phase.
       for (int x = max(0, c - S); x < c; ++x) {
         mbar_wait(&bars->k_full[x % S], (x / S) & 1, nullptr, kDrainBudget);
         mbar_wait(&bars->v_full[x % S], (x / S) & 1, nullptr, kDrainBudget);
       }
-      if (li > 0) mbar_wait(&bars->q_full, (li - 1) & 1, nullptr, kDrainBudget);
+      if constexpr (Cfg::kSepP) {
+        for (int g = 0; g < kQT; ++g)
+          if (qn[g] > 0) mbar_wait(&bars->q_full[g], (qn[g] - 1) & 1, nullptr, kDrainBudget);
+      } else {
+        if (li > 0) mbar_wait(&bars->q_full[0], (li - 1) & 1, nullptr, kDrainBudget);
+      }
     }
     __syncwarp();
-    } else if (warp == 1) {
-    // ======================= MMA issuer (whole warp, lane 0 issues) =======================
+    } else if (warp == 1 || (Cfg::kSepP && warp == 2)) {
+    // ================ MMA issuers (whole warp waits, lane 0 issues) ================
     {
       const uint32_t leader = (lane == 0) ? 1u : 0u;
       constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
@@ -287,17 +311,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_s = [&](int g, int s) {
         const uint64_t qa = dQ + ((g * Cfg::kTileBytes) >> 4);
         const uint64_t ka = dK + ((s * Cfg::kTileBytes) >> 4);
-        for (int kk = 0; kk < nks; ++kk)
-          mma_ss_w(tmem + g * kBN, qa + kstep(kk), ka + kstep(kk), kIdescQK, kk > 0, leader);
-        mma_commit_w(&bars->s_full[g], leader);
+        if (leader) {
+          for (int kk = 0; kk < nks; ++kk)
+            mma_ss(tmem + g * kBN, qa + kstep(kk), ka + kstep(kk), kIdescQK, kk > 0);
+          mma_commit(&bars->s_full[g]);
+        }
+        __syncwarp();
       };
       auto issue_pv = [&](int g, int s, bool acc) {
         const uint64_t va = dV + ((s * Cfg::kTileBytes) >> 4);
         const uint32_t pa = Cfg::kSepP ? tmem + 384 + g * 64 : tmem + g * kBN;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_w(tmem + 2 * kBN + g * DP, pa + kk * 8, va + ((kk * 2048) >> 4), kIdescPV,
-                   (acc || kk > 0) ? 1u : 0u, leader);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tmem + 2 * kBN + g * DP, pa + kk * 8, va + ((kk * 2048) >> 4), kIdescPV,
+                   (acc || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
       };
 
       int c = 0;                 // K/V blocks consumed so far (same count as the producer)
@@ -306,67 +336,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       int li = 0;
       bool ok = true;
       if constexpr (Cfg::kSepP) {
-        // S of a tile's block j+1 goes out as soon as its softmax has loaded S
-        // of block j; O += P V of block j as soon as P of block j is ready.
-        auto next_s = [&](int g, int s) -> bool {
-          if (sk[g] > 0 && !warp_wait(&bars->s_free[g], (sk[g] - 1) & 1, abort_flag, kWaitBudget))
-            return false;
-          tc_fence_after();
-          issue_s(g, s);
-          ++sk[g];
-          return true;
-        };
+        // One MMA warp per Q tile slot (g = warp - 1), so the two tiles never
+        // wait on each other's softmax.  Per block j of the tile: S(j) as soon
+        // as the softmax has S(j-1) in registers, then O += P(j-1) V(j-1) as
+        // soon as P(j-1) is in TMEM.  Every K/V stage gets one commit from
+        // each MMA warp (an empty one for blocks the tile does not visit).
+        const int g = warp - 1;
+        int qn = 0;
         for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
           const Item w = decode_item<kCausal>(it, nq, nk, H);
-          if (!warp_wait(&bars->q_full, li & 1, abort_flag, kWaitBudget) ||
-              !warp_wait(&bars->k_full[c % S], (c / S) & 1, abort_flag, kWaitBudget)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          for (int g = 0; g < kQT && ok; ++g)
-            if (w.nblk[g] > 0 && !next_s(g, c % S)) ok = false;
-          for (int j = 0; j < w.nmax && ok; ++j) {
-            const int cj = c + j, s = cj % S;
-            if (j + 1 < w.nmax) {
-              if (!warp_wait(&bars->k_full[(cj + 1) % S], ((cj + 1) / S) & 1, abort_flag,
-                             kWaitBudget)) {
-                ok = false;
-                break;
-              }
-              for (int g = 0; g < kQT && ok; ++g)
-                if (j + 1 < w.nblk[g] && !next_s(g, (cj + 1) % S)) ok = false;
-              if (!ok) break;
-            } else {
-              // every score MMA of this item has been issued: once they
-              // complete, the producer may load the next item's Q tiles
-              mma_commit_w(&bars->q_empty, leader);
-            }
-            if (!warp_wait(&bars->v_full[s], (cj / S) & 1, abort_flag, kWaitBudget)) {
+          const int nb = w.nblk[g];
+          if (nb > 0) {
+            if (!warp_wait(&bars->q_full[g], qn & 1, abort_flag, kWaitBudget)) {
               ok = false;
               break;
             }
-            for (int g = 0; g < kQT; ++g) {
-              if (j >= w.nblk[g]) continue;
-              if (!warp_wait(&bars->p_full[g], pc[g] & 1, abort_flag, kWaitBudget)) {
-                ok = false;
-                break;
-              }
-              ++pc[g];
-              tc_fence_after();
-              issue_pv(g, s, j > 0);
-              mma_commit_w(&bars->pv_done[g], leader);
-              if (j == w.nblk[g] - 1) mma_commit_w(&bars->o_final[g], leader);
-            }
-            if (!ok) break;
-            mma_commit_w(&bars->kv_empty[s], leader);
+            ++qn;
           }
+          auto pv_step = [&](int j) -> bool {   // O += P(j) V(j)
+            const int cj = c + j, s = cj % S;
+            if (!warp_wait(&bars->v_full[s], (cj / S) & 1, abort_flag, kWaitBudget) ||
+                !warp_wait(&bars->p_full[g], pc[g] & 1, abort_flag, kWaitBudget))
+              return false;
+            ++pc[g];
+            tc_fence_after();
+            issue_pv(g, s, j > 0);
+            mma_commit_w(&bars->pv_done[g], leader);
+            if (j == nb - 1) mma_commit_w(&bars->o_final[g], leader);
+            mma_commit_w(&bars->kv_empty[s], leader);
+            return true;
+          };
+          for (int j = 0; j < nb && ok; ++j) {
+            const int cj = c + j, s = cj % S;
+            if (!warp_wait(&bars->k_full[s], (cj / S) & 1, abort_flag, kWaitBudget) ||
+                (sk[g] > 0 &&
+                 !warp_wait(&bars->s_free[g], (sk[g] - 1) & 1, abort_flag, kWaitBudget))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(g, s);
+            ++sk[g];
+            // the tile's last scores are issued: once they complete, the
+            // producer may reload this Q slot
+            if (j == nb - 1) mma_commit_w(&bars->q_empty[g], leader);
+            if (j > 0 && !pv_step(j - 1)) ok = false;
+          }
+          if (ok && nb > 0 && !pv_step(nb - 1)) ok = false;
+          // Blocks this tile does not visit: commit only after the block has
+          // landed, so the commit counts toward this round of the stage and
+          // never toward the previous one (which the other MMA warp may still
+          // be reading).
+          for (int j = nb; j < w.nmax && ok; ++j) {
+            const int cj = c + j;
+            if (!warp_wait(&bars->k_full[cj % S], (cj / S) & 1, abort_flag, kWaitBudget)) {
+              ok = false;
+              break;
+            }
+            mma_commit_w(&bars->kv_empty[cj % S], leader);
+          }
+          if (!ok) break;
           c += w.nmax;
         }
       } else {
         for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
           const Item w = decode_item<kCausal>(it, nq, nk, H);
-          if (!warp_wait(&bars->q_full, li & 1, abort_flag, kWaitBudget) ||
+          if (!warp_wait(&bars->q_full[0], li & 1, abort_flag, kWaitBudget) ||
               !warp_wait(&bars->k_full[c % S], (c / S) & 1, abort_flag, kWaitBudget)) {
             ok = false;
             break;
@@ -382,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Every score MMA of this item has been issued by now: once they
             // complete, the producer may load the next item's Q tiles.
-            if (j == w.nmax - 1) mma_commit_w(&bars->q_empty, leader);
+            if (j == w.nmax - 1) mma_commit_w(&bars->q_empty[0], leader);
             bool k_next = false;
             for (int g = 0; g < kQT; ++g) {
               if (j >= w.nblk[g]) continue;
