@@ -79,16 +79,21 @@ struct FwdCfg {
   static constexpr int kChunks = DP / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kStages = (DP == 64) ? 4 : 2;
+  // separate-P layout: two Q buffers per tile slot (the next item's Q loads
+  // while this one runs) and a staging tile per slot for the TMA store of O
+  static constexpr int kQBufs = kSepP ? 2 : 1;
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQT * kTileBytes;
+  static constexpr int kKOff = kQOff + kQT * kQBufs * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kOOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kOOff + (kSepP ? kQT * kTileBytes : 0);
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // + barriers, + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per block");
 };
 
 struct FwdBars {
-  uint64_t q_full[kQT];    // separate-P layout: per tile; aliased layout: [0] for both
-  uint64_t q_empty[kQT];
+  uint64_t q_full[kQT][2];    // [slot][buffer]; aliased layout: [0][0] for both tiles
+  uint64_t q_empty[kQT][2];
   uint64_t k_full[4];
   uint64_t v_full[4];
   uint64_t kv_empty[4];
@@ -97,6 +102,8 @@ struct FwdBars {
   uint64_t p_full[kQT];
   uint64_t pv_done[kQT];   // O += P V of a block has completed (separate-P layout)
   uint64_t o_final[kQT];
+  uint64_t stage_free[kQT];   // O staging tile may be overwritten (separate-P layout)
+  uint64_t stage_full[kQT];   // O staging tile written by all 128 threads
   uint64_t drain;
   uint64_t probe;
   uint32_t tmem_base;
@@ -159,7 +166,8 @@ __device__ __forceinline__ int item_index(int li, int num_items) {
 template <int DP, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FwdParams p) {
   using Cfg = FwdCfg<DP>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -178,13 +186,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int g = 0; g < kQT; ++g) {
-      mbar_init(&bars->q_full[g], 1);
-      mbar_init(&bars->q_empty[g], 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bars->q_full[g][b], 1);
+        mbar_init(&bars->q_empty[g][b], 1);
+      }
       mbar_init(&bars->s_full[g], 1);
       mbar_init(&bars->s_free[g], kBM);
       mbar_init(&bars->p_full[g], kBM);
       mbar_init(&bars->pv_done[g], 1);
       mbar_init(&bars->o_final[g], 1);
+      mbar_init(&bars->stage_free[g], 1);
+      mbar_init(&bars->stage_full[g], kBM);
     }
     for (int s = 0; s < S; ++s) {
       mbar_init(&bars->k_full[s], 1);
@@ -217,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + Cfg::kQOff;
   uint8_t* sK = smem + Cfg::kKOff;
   uint8_t* sV = smem + Cfg::kVOff;
+  uint8_t* sO = smem + Cfg::kOOff;
 
   // Role bodies; each runs inside the branch that sets its register budget.
   auto load_roles = [&](int warp, int lane) {
@@ -228,36 +241,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmV);
       int c = 0;             // K/V blocks issued so far
       int li = 0;            // items started by this CTA
-      int qn[kQT] = {0, 0};  // Q loads per tile slot (separate-P layout)
       bool ok = true;
       for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(li, num_items)) {
         const Item w = decode_item<kCausal>(it, nq, nk, H);
-        if constexpr (Cfg::kSepP) {
-          // each tile slot's Q is reloaded once its previous scores are done
-          for (int g = 0; g < kQT && ok; ++g) {
-            if (w.tile[g] < 0) continue;
-            if (qn[g] > 0 &&
-                !mbar_wait(&bars->q_empty[g], (qn[g] - 1) & 1, abort_flag, kWaitBudget)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&bars->q_full[g], Cfg::kTileBytes);
-            for (int ch = 0; ch < Cfg::kChunks; ++ch)
-              tma_load_4d(sQ + g * Cfg::kTileBytes + ch * kChunkBytes, &tmQ, &bars->q_full[g],
-                          ch * 64, w.h, w.tile[g] * kBM, w.b);
-            ++qn[g];
-          }
-          if (!ok) break;
-        } else {
-          if (li > 0 && !mbar_wait(&bars->q_empty[0], (li - 1) & 1, abort_flag, kWaitBudget)) {
+        if constexpr (!Cfg::kSepP) {   // separate-P layout: Q comes from warp 3
+          if (li > 0 && !mbar_wait(&bars->q_empty[0][0], (li - 1) & 1, abort_flag, kWaitBudget)) {
             ok = false;
             break;
           }
           const int nact = (w.tile[1] < 0) ? 1 : 2;
-          mbar_arrive_expect_tx(&bars->q_full[0], nact * Cfg::kTileBytes);
+          mbar_arrive_expect_tx(&bars->q_full[0][0], nact * Cfg::kTileBytes);
           for (int g = 0; g < nact; ++g)
             for (int ch = 0; ch < Cfg::kChunks; ++ch)
-              tma_load_4d(sQ + g * Cfg::kTileBytes + ch * kChunkBytes, &tmQ, &bars->q_full[0],
+              tma_load_4d(sQ + g * Cfg::kTileBytes + ch * kChunkBytes, &tmQ, &bars->q_full[0][0],
                           ch * 64, w.h, w.tile[g] * kBM, w.b);
         }
         ++li;
@@ -286,12 +282,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bars->k_full[x % S], (x / S) & 1, nullptr, kDrainBudget);
         mbar_wait(&bars->v_full[x % S], (x / S) & 1, nullptr, kDrainBudget);
       }
-      if constexpr (Cfg::kSepP) {
-        for (int g = 0; g < kQT; ++g)
-          if (qn[g] > 0) mbar_wait(&bars->q_full[g], (qn[g] - 1) & 1, nullptr, kDrainBudget);
-      } else {
-        if (li > 0) mbar_wait(&bars->q_full[0], (li - 1) & 1, nullptr, kDrainBudget);
+      if (!Cfg::kSepP && li > 0)
+        mbar_wait(&bars->q_full[0][0], (li - 1) & 1, nullptr, kDrainBudget);
+    }
+    __syncwarp();
+    } else if (Cfg::kSepP && warp == 3) {
+    // ============ Q producer (separate-P layout): two buffers per tile slot ============
+    if (lane == 0) {
+      int li = 0;
+      int qn[kQT] = {0, 0};   // Q loads per slot; load n uses buffer n & 1
+      bool ok = true;
+      for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
+        const Item w = decode_item<kCausal>(it, nq, nk, H);
+        for (int g = 0; g < kQT; ++g) {
+          if (w.tile[g] < 0) continue;
+          const int b = qn[g] & 1, u = qn[g] >> 1;
+          // the buffer's previous use (load n - 2) has had all its scores computed
+          if (u > 0 &&
+              !mbar_wait(&bars->q_empty[g][b], (u - 1) & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->q_full[g][b], Cfg::kTileBytes);
+          for (int ch = 0; ch < Cfg::kChunks; ++ch)
+            tma_load_4d(sQ + (g * 2 + b) * Cfg::kTileBytes + ch * kChunkBytes, &tmQ,
+                        &bars->q_full[g][b], ch * 64, w.h, w.tile[g] * kBM, w.b);
+          ++qn[g];
+        }
       }
+      if (!ok) raise_abort(bars, p.status);
+      for (int g = 0; g < kQT; ++g)
+        for (int n = max(0, qn[g] - 2); n < qn[g]; ++n)
+          mbar_wait(&bars->q_full[g][n & 1], (n >> 1) & 1, nullptr, kDrainBudget);
     }
     __syncwarp();
     } else if (warp == 1 || (Cfg::kSepP && warp == 2)) {
@@ -308,8 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto kstep = [](int kk) -> uint64_t {
         return static_cast<uint64_t>(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
       };
-      auto issue_s = [&](int g, int s) {
-        const uint64_t qa = dQ + ((g * Cfg::kTileBytes) >> 4);
+      // scores of tile g from the Q tile at index qi (slot-major, then buffer)
+      auto issue_s = [&](int g, int qi, int s) {
+        const uint64_t qa = dQ + ((qi * Cfg::kTileBytes) >> 4);
         const uint64_t ka = dK + ((s * Cfg::kTileBytes) >> 4);
         if (leader) {
           for (int kk = 0; kk < nks; ++kk)
@@ -346,8 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
           const Item w = decode_item<kCausal>(it, nq, nk, H);
           const int nb = w.nblk[g];
+          const int qb = qn & 1;   // Q buffer of this item (its load number is qn)
           if (nb > 0) {
-            if (!warp_wait(&bars->q_full[g], qn & 1, abort_flag, kWaitBudget)) {
+            if (!warp_wait(&bars->q_full[g][qb], (qn >> 1) & 1, abort_flag, kWaitBudget)) {
               ok = false;
               break;
             }
@@ -375,11 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            issue_s(g, s);
+            issue_s(g, g * 2 + qb, s);
             ++sk[g];
             // the tile's last scores are issued: once they complete, the
-            // producer may reload this Q slot
-            if (j == nb - 1) mma_commit_w(&bars->q_empty[g], leader);
+            // producer may reload this Q buffer
+            if (j == nb - 1) mma_commit_w(&bars->q_empty[g][qb], leader);
             if (j > 0 && !pv_step(j - 1)) ok = false;
           }
           if (ok && nb > 0 && !pv_step(nb - 1)) ok = false;
@@ -401,14 +425,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
           const Item w = decode_item<kCausal>(it, nq, nk, H);
-          if (!warp_wait(&bars->q_full[0], li & 1, abort_flag, kWaitBudget) ||
+          if (!warp_wait(&bars->q_full[0][0], li & 1, abort_flag, kWaitBudget) ||
               !warp_wait(&bars->k_full[c % S], (c / S) & 1, abort_flag, kWaitBudget)) {
             ok = false;
             break;
           }
           tc_fence_after();
           for (int g = 0; g < kQT; ++g)
-            if (w.nblk[g] > 0) issue_s(g, c % S);
+            if (w.nblk[g] > 0) issue_s(g, g, c % S);
           for (int j = 0; j < w.nmax; ++j) {
             const int cj = c + j, s = cj % S;
             if (!warp_wait(&bars->v_full[s], (cj / S) & 1, abort_flag, kWaitBudget)) {
@@ -417,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Every score MMA of this item has been issued by now: once they
             // complete, the producer may load the next item's Q tiles.
-            if (j == w.nmax - 1) mma_commit_w(&bars->q_empty[0], leader);
+            if (j == w.nmax - 1) mma_commit_w(&bars->q_empty[0][0], leader);
             bool k_next = false;
             for (int g = 0; g < kQT; ++g) {
               if (j >= w.nblk[g]) continue;
@@ -438,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   tc_fence_after();
                   k_next = true;
                 }
-                issue_s(g, (cj + 1) % S);
+                issue_s(g, g, (cj + 1) % S);
               } else {
                 mma_commit_w(&bars->o_final[g], leader);
               }
@@ -622,30 +646,85 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live = l > 0.0f;
       const float inv = live ? 1.0f / l : 0.0f;
       const bool store = q_row < N;
-      __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
-      uint4* orow = reinterpret_cast<uint4*>(
-          O + ((static_cast<size_t>(w.b) * N + (store ? q_row : 0)) * H + w.h) * p.d);
+      if constexpr (Cfg::kSepP) {
+        // Stage the bf16 O tile in shared memory in the TMA box layout (rows
+        // of 128 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7)), then
+        // one thread stores it with a TMA tensor store (rows >= N and columns
+        // >= d are not written).  The staging tile is reused once the previous
+        // store has read it.
+        // (mbarrier handshakes, so that every wait is bounded)
+        uint8_t* stage = sO + g * Cfg::kTileBytes;
+        const int e = oc - 1;   // epilogues of this slot so far
+        if (row == 0) {
+          bulk_wait_read_all();
+          mbar_arrive(&bars->stage_free[g]);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->stage_free[g], e & 1, abort_flag,
+                                               kWaitBudget))) {
+          ok = false;
+          break;
+        }
 #pragma unroll
-      for (int cc = 0; cc < DP / 32; ++cc) {
-        uint32_t orr[32];
-        __syncwarp();   // the stores below are per-thread; tcgen05.ld is collective
-        tmem_ld32(tO + cc * 32, orr);
-        tmem_ld_wait(orr);
-        if (store) {
+        for (int cc = 0; cc < DP / 32; ++cc) {
+          uint32_t orr[32];
+          __syncwarp();   // tcgen05.ld is warp-collective
+          tmem_ld32(tO + cc * 32, orr);
+          tmem_ld_wait(orr);
 #pragma unroll
           for (int qv = 0; qv < 4; ++qv) {
-            const int col = cc * 32 + qv * 8;
-            if (col < p.d) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(orr[qv * 8 + 0]) * inv,
-                                __uint_as_float(orr[qv * 8 + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(orr[qv * 8 + 2]) * inv,
-                                __uint_as_float(orr[qv * 8 + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(orr[qv * 8 + 4]) * inv,
-                                __uint_as_float(orr[qv * 8 + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(orr[qv * 8 + 6]) * inv,
-                                __uint_as_float(orr[qv * 8 + 7]) * inv);
-              orow[col / 8] = v;
+            const int chunk = cc * 4 + qv;   // 16-byte chunk of the row (8 columns)
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(orr[qv * 8 + 0]) * inv,
+                              __uint_as_float(orr[qv * 8 + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(orr[qv * 8 + 2]) * inv,
+                              __uint_as_float(orr[qv * 8 + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(orr[qv * 8 + 4]) * inv,
+                              __uint_as_float(orr[qv * 8 + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(orr[qv * 8 + 6]) * inv,
+                              __uint_as_float(orr[qv * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4)) = v;
+          }
+        }
+        fence_proxy_async_smem();   // the TMA engine reads what the threads wrote
+        mbar_arrive(&bars->stage_full[g]);
+        if (row == 0) {
+          if (!mbar_wait(&bars->stage_full[g], e & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+          } else {
+            tma_store_4d(&tmO, stage, 0, w.h, qt * kBM, w.b);
+            bulk_commit_group();
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+      } else {
+        __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
+        uint4* orow = reinterpret_cast<uint4*>(
+            O + ((static_cast<size_t>(w.b) * N + (store ? q_row : 0)) * H + w.h) * p.d);
+#pragma unroll
+        for (int cc = 0; cc < DP / 32; ++cc) {
+          uint32_t orr[32];
+          __syncwarp();   // the stores below are per-thread; tcgen05.ld is collective
+          tmem_ld32(tO + cc * 32, orr);
+          tmem_ld_wait(orr);
+          if (store) {
+#pragma unroll
+            for (int qv = 0; qv < 4; ++qv) {
+              const int col = cc * 32 + qv * 8;
+              if (col < p.d) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(orr[qv * 8 + 0]) * inv,
+                                  __uint_as_float(orr[qv * 8 + 1]) * inv);
+                v.y = pack_bf16x2(__uint_as_float(orr[qv * 8 + 2]) * inv,
+                                  __uint_as_float(orr[qv * 8 + 3]) * inv);
+                v.z = pack_bf16x2(__uint_as_float(orr[qv * 8 + 4]) * inv,
+                                  __uint_as_float(orr[qv * 8 + 5]) * inv);
+                v.w = pack_bf16x2(__uint_as_float(orr[qv * 8 + 6]) * inv,
+                                  __uint_as_float(orr[qv * 8 + 7]) * inv);
+                orow[col / 8] = v;
+              }
             }
           }
         }
@@ -656,6 +735,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             live ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
     if (!ok) raise_abort(bars, p.status);
+    // the O stores must have completed (and read shared memory) before exit
+    if (Cfg::kSepP && row == 0) bulk_wait_all();
     __syncwarp();
   };
 
@@ -686,10 +767,11 @@ int sm_count() {
 template <int DP, bool kCausal>
 cudaError_t launch_tc(const FwdParams& p, cudaStream_t st) {
   using Cfg = FwdCfg<DP>;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   cudaError_t e = make_bhnd_tmap(&mq, p.q, p.B, p.N, p.H, p.d);
   if (e == cudaSuccess) e = make_bhnd_tmap(&mk, p.k, p.B, p.N, p.H, p.d);
   if (e == cudaSuccess) e = make_bhnd_tmap(&mv, p.v, p.B, p.N, p.H, p.d);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&mo, p.o, p.B, p.N, p.H, p.d);
   if (e != cudaSuccess) return e;
   auto kern = fwd_tc_kernel<DP, kCausal>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
@@ -701,7 +783,7 @@ cudaError_t launch_tc(const FwdParams& p, cudaStream_t st) {
   if (sms <= 0) return cudaErrorInvalidDevice;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   FwdParams pc = p;
-  void* args[] = {&mq, &mk, &mv, &pc};
+  void* args[] = {&mq, &mk, &mv, &mo, &pc};
   return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads), args,
                           Cfg::kSmemBytes, st);
 }
