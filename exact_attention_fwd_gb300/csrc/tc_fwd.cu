@@ -46,6 +46,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <cfloat>
 #include <cmath>
 
 #include "fa_common.cuh"
@@ -201,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], Cfg::kSepP ? kQT : 1);   // one commit per MMA warp
+      // separate-P layout: one arrival per softmax warpgroup; else one commit
+      mbar_init(&bars->kv_empty[s], Cfg::kSepP ? kQT : 1);
     }
     mbar_init(&bars->drain, Cfg::kSepP ? kQT : 1);   // one commit per MMA warp
     mbar_init(&bars->probe, 1);
@@ -320,7 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================ MMA issuers (whole warp waits, lane 0 issues) ================
     {
       const uint32_t leader = (lane == 0) ? 1u : 0u;
-      constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
+      // A negative scale is applied as a sign flip of Q inside the score MMA
+      // (instruction-descriptor bit 13, negate A), so the softmax always
+      // works with a positive scale.
+      const uint32_t kIdescQK =
+          idesc_bf16(kBM, kBN, false, false) | (p.scale_log2 < 0.0f ? (1u << 13) : 0u);
       constexpr uint32_t kIdescPV = idesc_bf16(kBM, DP, false, true);
       const int nks = (p.d + 15) / 16;       // K=16 steps over the head dim
       // Descriptor bases; K steps and stages advance the start-address field.
@@ -362,8 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One MMA warp per Q tile slot (g = warp - 1), so the two tiles never
         // wait on each other's softmax.  Per block j of the tile: S(j) as soon
         // as the softmax has S(j-1) in registers, then O += P(j-1) V(j-1) as
-        // soon as P(j-1) is in TMEM.  Every K/V stage gets one commit from
-        // each MMA warp (an empty one for blocks the tile does not visit).
+        // soon as P(j-1) is in TMEM.  One commit per MMA group (each costs
+        // tensor-pipe time): s_full after S, pv_done after PV; the softmax
+        // warpgroup releases K/V stages once it has seen the PV complete.
         const int g = warp - 1;
         int qn = 0;
         for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
@@ -386,8 +393,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_pv(g, s, j > 0);
             mma_commit_w(&bars->pv_done[g], leader);
-            if (j == nb - 1) mma_commit_w(&bars->o_final[g], leader);
-            mma_commit_w(&bars->kv_empty[s], leader);
             return true;
           };
           for (int j = 0; j < nb && ok; ++j) {
@@ -407,18 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j > 0 && !pv_step(j - 1)) ok = false;
           }
           if (ok && nb > 0 && !pv_step(nb - 1)) ok = false;
-          // Blocks this tile does not visit: commit only after the block has
-          // landed, so the commit counts toward this round of the stage and
-          // never toward the previous one (which the other MMA warp may still
-          // be reading).
-          for (int j = nb; j < w.nmax && ok; ++j) {
-            const int cj = c + j;
-            if (!warp_wait(&bars->k_full[cj % S], (cj / S) & 1, abort_flag, kWaitBudget)) {
-              ok = false;
-              break;
-            }
-            mma_commit_w(&bars->kv_empty[cj % S], leader);
-          }
           if (!ok) break;
           c += w.nmax;
         }
@@ -491,16 +484,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + g * kBN;
     const uint32_t tO = tmem + lane_base + 2 * kBN + g * DP;
     const uint32_t tP = tmem + lane_base + 384 + g * 64;   // separate-P layout only
-    const float c = p.scale_log2;
+    // |scale| log2(e): a negative scale reaches the softmax as negated scores
+    // (see the score MMA); a zero scale, whose weights are uniform over the
+    // unmasked keys, as the smallest positive normal float, which makes every
+    // exponent 2^(s c - m) round to 1 while masked keys (-inf) still give 0.
+    const float c = p.scale_log2 > 0.0f ? p.scale_log2
+                                        : (p.scale_log2 < 0.0f ? -p.scale_log2 : FLT_MIN);
     int sc = 0;    // s_full phases consumed
-    int oc = 0;    // o_final phases consumed
+    int oc = 0;    // epilogues done (o_final phases consumed)
+    int kc = 0;    // K/V blocks of the items before this one (separate-P layout)
     bool ok = true;
+    // Separate-P layout: this warpgroup's release of the K/V stage of global
+    // block x, once its own MMAs no longer read it.  For a block the tile does
+    // not visit, the release waits until the block has landed, so it counts
+    // toward that round of the stage and never toward the previous one.
+    auto release_kv = [&](int x, bool wait_landed) -> bool {
+      if (wait_landed &&
+          !__all_sync(0xffffffffu, mbar_wait(&bars->k_full[x % S], (x / S) & 1, abort_flag,
+                                             kWaitBudget)))
+        return false;
+      if (row == 0) mbar_arrive(&bars->kv_empty[x % S]);
+      return true;
+    };
 
     int li = 0;
     for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
       const Item w = decode_item<kCausal>(it, nq, nk, H);
       const int qt = w.tile[g];
-      if (qt < 0) continue;
+      if (qt < 0) {
+        if constexpr (Cfg::kSepP) {
+          for (int j = 0; j < w.nmax && ok; ++j) ok = release_kv(kc + j, true);
+          kc += w.nmax;
+        }
+        continue;
+      }
       const int q_row = qt * kBM + row;
       float m_ref = -INFINITY;   // reference max of the scaled scores, log2 units
       float l = 0.0f;
@@ -530,41 +547,57 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars->s_free[g]);
         }
 
-        // One code path for every block (the instruction cache holds one copy
-        // of the unrolled row loops): blocks with masked keys, and the rare
-        // non-positive scale, first scale the row in place and set masked
-        // keys to -inf; the common case folds the scale into the exponent.
-        const bool masked = (kCausal && j == qt) || ((j + 1) * kBN > N);
-        float c_eff = c;
-        if (masked || !(c > 0.0f)) {
+        // Blocks with masked keys (the diagonal block of a causal tile, the
+        // ragged last block) set them to -inf before the row max: key k0 + i
+        // is masked when i > lim (beyond N, or after q_row).  One copy of the
+        // row loops serves every block (the instruction cache holds it once).
+        if ((kCausal && j == qt) || ((j + 1) * kBN > N)) {
           const int k0 = j * kBN;
+          const int lim = min(N - k0 - 1, kCausal ? q_row - k0 : kBN);
 #pragma unroll
-          for (int i = 0; i < kBN; ++i) {
-            const bool bad = (k0 + i >= N) || (kCausal && k0 + i > q_row);
-            s[i] = bad ? -INFINITY : s[i] * c;
-          }
-          c_eff = 1.0f;
+          for (int i = 0; i < kBN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
         }
-        float m_blk;
-        {
-          float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < kBN; i += 8) {   // four chains, columns 0 .. kBN-1
-            a0 = fmax3(a0, s[i], s[i + 1]);
-            a1 = fmax3(a1, s[i + 2], s[i + 3]);
-            a2 = fmax3(a2, s[i + 4], s[i + 5]);
-            a3 = fmax3(a3, s[i + 6], s[i + 7]);
-          }
-          m_blk = fmax3(a0, a1, fmaxf(a2, a3)) * c_eff;
-        }
-
-        // Lazy rescale: move the reference max only when it rises enough.
-        const bool rise = (m_ref == -INFINITY) ? (m_blk != -INFINITY)
-                                               : (m_blk > m_ref + kRescaleThreshold);
+        bool rise = false;
         float alpha = 1.0f;
-        if (rise) {
-          alpha = (m_ref == -INFINITY) ? 0.0f : fast_exp2(m_ref - m_blk);
-          m_ref = m_blk;
+        uint32_t pk[kBN / 2];
+        {
+          float m_blk;
+          {
+            float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kBN; i += 8) {   // four chains, columns 0 .. kBN-1
+              a0 = fmax3(a0, s[i], s[i + 1]);
+              a1 = fmax3(a1, s[i + 2], s[i + 3]);
+              a2 = fmax3(a2, s[i + 4], s[i + 5]);
+              a3 = fmax3(a3, s[i + 6], s[i + 7]);
+            }
+            m_blk = fmax3(a0, a1, fmaxf(a2, a3)) * c;
+          }
+          // Lazy rescale: move the reference max only when it rises enough.
+          rise = (m_ref == -INFINITY) ? (m_blk != -INFINITY)
+                                      : (m_blk > m_ref + kRescaleThreshold);
+          if (rise) {
+            alpha = (m_ref == -INFINITY) ? 0.0f : fast_exp2(m_ref - m_blk);
+            m_ref = m_blk;
+          }
+          l *= alpha;
+          const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+          const uint64_t negm2 = f2_pack(-m_use, -m_use);
+          const uint64_t c2 = f2_pack(c, c);
+          // P = 2^(s c - m) as bf16 pairs.
+          uint64_t lsum0 = 0, lsum1 = 0;   // two packed partial sums (+0.0f pairs)
+#pragma unroll
+          for (int i = 0; i < kBN / 2; ++i) {
+            const uint64_t sv = f2_pack(s[2 * i], s[2 * i + 1]);
+            const uint64_t t = f2_fma(sv, c2, negm2);
+            const float p0 = fast_exp2(f2_lo(t));
+            const float p1 = fast_exp2(f2_hi(t));
+            const uint64_t pp = f2_pack(p0, p1);
+            if (i & 1) lsum1 = f2_add(lsum1, pp); else lsum0 = f2_add(lsum0, pp);
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          const uint64_t ls = f2_add(lsum0, lsum1);
+          l += f2_lo(ls) + f2_hi(ls);
         }
         const bool rescale = j > 0 && __any_sync(0xffffffffu, rise);
         // O row *= alpha in TMEM (warp-collective; alpha is 1 in rows whose
@@ -590,26 +623,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Aliased layout: PV of block j-1 has completed, since the s_full
         // commit of block j came after it.
         if (!Cfg::kSepP && rescale) rescale_o();
-        l *= alpha;
-        const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
-        const uint64_t negm2 = f2_pack(-m_use, -m_use);
-        const uint64_t ce2 = f2_pack(c_eff, c_eff);
-
-        // P = 2^(s c - m) as bf16 pairs.
-        uint64_t lsum0 = 0, lsum1 = 0;   // two packed partial sums (+0.0f pairs)
-        uint32_t pk[kBN / 2];
-#pragma unroll
-        for (int i = 0; i < kBN / 2; ++i) {
-          const uint64_t sv = f2_pack(s[2 * i], s[2 * i + 1]);
-          const uint64_t t = f2_fma(sv, ce2, negm2);
-          const float p0 = fast_exp2(f2_lo(t));
-          const float p1 = fast_exp2(f2_hi(t));
-          const uint64_t pp = f2_pack(p0, p1);
-          if (i & 1) lsum1 = f2_add(lsum1, pp); else lsum0 = f2_add(lsum0, pp);
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        const uint64_t ls = f2_add(lsum0, lsum1);
-        l += f2_lo(ls) + f2_hi(ls);
         if constexpr (Cfg::kSepP) {
           // P_g and O_g are free once PV of the previous block has completed
           // (the pv_done phase of that block; blocks counted across items).
@@ -619,6 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // block j-1's MMAs are done (the previous item's last block was
+          // released by that item's epilogue)
+          if (j > 0) release_kv(kc + j - 1, false);
           tc_fence_after();
           if (rescale) rescale_o();
           __syncwarp();
@@ -636,12 +652,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---- epilogue: O / l -> bf16, L = (m + log2 l) ln 2 ----
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_final[g], oc & 1, abort_flag,
-                                             kWaitBudget))) {
+      // Separate-P layout: the last block's pv_done phase (its PV is the
+      // tile's last MMA); then the item's remaining K/V stages are released.
+      if (!__all_sync(0xffffffffu,
+                      Cfg::kSepP
+                          ? mbar_wait(&bars->pv_done[g], (sc - 1) & 1, abort_flag, kWaitBudget)
+                          : mbar_wait(&bars->o_final[g], oc & 1, abort_flag, kWaitBudget))) {
         ok = false;
         break;
       }
       ++oc;
+      if constexpr (Cfg::kSepP) {
+        release_kv(kc + w.nblk[g] - 1, false);
+        for (int j = w.nblk[g]; j < w.nmax && ok; ++j) ok = release_kv(kc + j, true);
+        kc += w.nmax;
+        if (!ok) break;
+      }
       tc_fence_after();
       const bool live = l > 0.0f;
       const float inv = live ? 1.0f / l : 0.0f;
