@@ -506,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dd = p.D[hb + q];
               }
             }
-            vec[col] = l2;
-            vec[kBlk + col] = dd;
+            vec[col] = -l2;          // stored negated: the exponent is s c + (-L2)
+            vec[kBlk + col] = -dd;
           }
           mbar_arrive(&bars->vec_full[s]);
         }
@@ -608,40 +608,57 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars->sp_free);
         }
         const int col0 = (w.i0 + t) * kBlk + colg;   // first query (dK/dV) or key (dQ)
-        bool masked;
-        if (kDkDv) masked = kCausal && (col0 < w.row0 + kRows - 1);
-        else masked = (kCausal && (col0 + 63 > w.row0)) || (col0 + 64 > N);
-        const float* vec = kDkDv ? stage_vec(s) + colg : nullptr;
+        // Masked pairs get s = -inf before the exponent (P = 0, dS = 0): a
+        // select against a per-row column limit, in blocks that need it.
+        //   dK/dV (row = key, column = query): masked when query < key.
+        //   dQ (row = query, column = key): masked when key > query or key >= N.
+        // Queries >= N in the dK/dV kernel carry -L2 = -inf, which also gives 0.
+        if (kDkDv) {
+          if (kCausal && col0 < w.row0 + kRows - 1) {
+            const int lim = grow - col0;   // columns cl < lim are masked
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              sr[i] = (i < lim) ? __float_as_uint(-INFINITY) : sr[i];
+          }
+        } else if ((kCausal && col0 + 63 > w.row0) || (col0 + 64 > N)) {
+          const int lim = min(kCausal ? grow - col0 : 64, N - 1 - col0);   // cl > lim masked
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            sr[i] = (i > lim) ? __float_as_uint(-INFINITY) : sr[i];
+        }
+        // Element-wise math on packed pairs (f32x2): t = s c - L2,
+        // P = 2^t, dS = P (dP - D); the dQ kernel also sums P dP per row.
+        const float2* nl2v = kDkDv ? reinterpret_cast<const float2*>(stage_vec(s) + colg) : nullptr;
+        const float2* ndv = kDkDv ? reinterpret_cast<const float2*>(stage_vec(s) + kBlk + colg)
+                                  : nullptr;
+        const uint64_t c2 = f2_pack(c, c);
+        const uint64_t nl2_row = f2_pack(-l2_row, -l2_row);
+        const uint64_t nd_row = f2_pack(-d_row, -d_row);
+        uint64_t dacc2 = 0;   // (+0.0f, +0.0f)
         uint32_t pk[32], dk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          float pp[2], ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cl = 2 * i + e;                // column within this warpgroup's 64
-            const float sv = __uint_as_float(sr[cl]);
-            const float dpv = __uint_as_float(dr[cl]);
-            float l2, dd;
-            if (kDkDv) {
-              l2 = vec[cl];
-              dd = vec[kBlk + cl];
-            } else {
-              l2 = l2_row;
-              dd = d_row;
-            }
-            float pv = fast_exp2(fmaf(sv, c, -l2));
-            if (masked) {
-              const int other = col0 + cl;
-              const bool bad = kDkDv ? (other < grow) : ((kCausal && other > grow) || other >= N);
-              if (bad) pv = 0.0f;
-            }
-            if (!kDkDv) d_acc = fmaf(pv, dpv, d_acc);
-            pp[e] = pv;
-            ds[e] = pv * (dpv - dd);
+          uint64_t nl2, nd;
+          if (kDkDv) {
+            const float2 a = nl2v[i], bq = ndv[i];
+            nl2 = f2_pack(a.x, a.y);
+            nd = f2_pack(bq.x, bq.y);
+          } else {
+            nl2 = nl2_row;
+            nd = nd_row;
           }
-          pk[i] = kDkDv ? pack_bf16x2(pp[0], pp[1]) : pack_f16x2(pp[0], pp[1]);
-          dk[i] = pack_f16x2(ds[0], ds[1]);
+          const uint64_t s2 = f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+          const uint64_t dp2 = f2_pack(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]));
+          const uint64_t t2 = f2_fma(s2, c2, nl2);
+          const float p0 = fast_exp2(f2_lo(t2));
+          const float p1 = fast_exp2(f2_hi(t2));
+          const uint64_t p2 = f2_pack(p0, p1);
+          if (!kDkDv) dacc2 = f2_fma(p2, dp2, dacc2);
+          const uint64_t ds2 = f2_mul(p2, f2_add(dp2, nd));
+          pk[i] = kDkDv ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+          dk[i] = pack_f16x2(f2_lo(ds2), f2_hi(ds2));
         }
+        if (!kDkDv) d_acc += f2_lo(dacc2) + f2_hi(dacc2);
         if (kWide) {
           // P and dS columns are free once the previous block's accumulating
           // MMAs have completed
