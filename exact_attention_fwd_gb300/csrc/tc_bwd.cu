@@ -72,6 +72,10 @@ namespace {
 
 constexpr int kRows = 128;       // rows owned by a work item
 constexpr int kThreads = 384;
+constexpr int kRegsHelper = 80;    // warps 0-3: TMA, MMA, vectors, fp16 copy
+constexpr int kRegsElem = 208;     // warps 4-11: element-wise and epilogue
+static_assert(4 * 32 * kRegsHelper + 8 * 32 * kRegsElem <= 168 * kThreads,
+              "register split exceeds the launch allocation");
 constexpr int kTmemCols = 512;
 constexpr int kStagesMax = 3;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -255,22 +259,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->r_empty, 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(&bars->c_full[s], 1);
-      mbar_init(&bars->c_empty[s], 1);
+      mbar_init(&bars->c_empty[s], kWide ? 2 : 1);   // one commit per MMA warp
       mbar_init(&bars->vec_full[s], 32);
       mbar_init(&bars->conv_full[s], 32);
     }
     mbar_init(&bars->sp_full, 1);
     mbar_init(&bars->sp_free, 256);
     mbar_init(&bars->pd_full, 256);
-    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->acc_done, 2);   // wide layout: one commit per MMA warp
     for (int g = 0; g < 2; ++g) {
       mbar_init(&bars->s_full[g], 1);
       mbar_init(&bars->p_full[g], 128);
     }
-    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_full, kWide ? 2 : 1);
     mbar_init(&bars->acc_free, 256);
     mbar_init(&bars->dsum, 256);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, kWide ? 2 : 1);
     mbar_init(&bars->probe, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -301,6 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     return reinterpret_cast<float*>(stage_c1(s) + 3 * Cfg::kBlkTile);
   };
 
+  // Role bodies; each runs inside the branch that sets its register budget
+  // (setmaxnreg: the element-wise warps hold S, dP, P and dS of a row).
+  auto helper_roles = [&]() {
   if (run && warp == 0) {
     // ======================= TMA producer =======================
     if (lane == 0) {
@@ -346,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (li > 0) mbar_wait(&bars->r_full, (li - 1) & 1, nullptr, kDrainBudget);
     }
     __syncwarp();
-  } else if (run && warp == 1) {
-    // ============ MMA issuer (whole warp converged, lane 0 issues) ============
+  } else if (run && (warp == 1 || (kWide && warp == 2))) {
+    // ============ MMA issuers (whole warp waits, lane 0 issues) ============
     const uint32_t leader = (lane == 0) ? 1u : 0u;
     constexpr uint32_t kIdescSP = idesc_bf16(kRows, kBlk, false, false);
     constexpr uint32_t kIdescAccBf = idesc_bf16(kRows, DP, false, true);
@@ -359,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dC1 = sdesc_sw128(smem_u32(stage_c1(0)), 16, 1024);
     const uint64_t dC2 = sdesc_sw128(smem_u32(stage_c2(0)), 16, 1024);
     const uint64_t dC1hMN = sdesc_sw128(smem_u32(stage_c1h(0)), Cfg::kBlkChunk, 1024);
+    const uint64_t dC1MN = sdesc_sw128(smem_u32(stage_c1(0)), Cfg::kBlkChunk, 1024);
     const uint64_t dC2MN = sdesc_sw128(smem_u32(stage_c2(0)), Cfg::kBlkChunk, 1024);
 
     // S and dP of global block cb into TMEM column offset `col`
@@ -374,8 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    // accumulating MMAs of global block cb; P and dS at TMEM columns pcol, dcol
-    auto issue_acc = [&](int cb, bool first, uint32_t pcol, uint32_t dcol) {
+    // accumulating MMAs of global block cb; P and dS at TMEM columns pcol,
+    // dcol.  parts: 1 = acc1 only, 2 = acc2 only, 3 = both (interleaved).
+    //   acc1: dV += P dO_i (bf16)  or  B += P K_j (fp16)
+    //   acc2: dK += dS Q_i         or  dQ += dS K_j   (fp16)
+    auto issue_acc = [&](int cb, bool first, uint32_t pcol, uint32_t dcol, int parts) {
       const uint64_t so = static_cast<uint64_t>(((cb % S) * Cfg::kStageBytes) >> 4);
       if (leader) {
 #pragma unroll
@@ -384,12 +395,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t pa = tmem + pcol + kk * 8;
           const uint32_t da = tmem + dcol + kk * 8;
           const uint64_t ko = static_cast<uint64_t>((kk * 2048) >> 4);
-          if (kDkDv)  // dV += P dO_i (bf16)
-            mma_ts(tmem + Cfg::kTAcc1, pa, dC2MN + so + ko, kIdescAccBf, acc);
-          else        // B += P K_j (fp16)
-            mma_ts(tmem + Cfg::kTAcc1, pa, dC1hMN + so + ko, kIdescAccH, acc);
-          // dK += dS Q_i   or   dQ += dS K_j   (fp16)
-          mma_ts(tmem + Cfg::kTAcc2, da, dC1hMN + so + ko, kIdescAccH, acc);
+          if (parts & 1) {
+            if (kDkDv)
+              mma_ts(tmem + Cfg::kTAcc1, pa, dC2MN + so + ko, kIdescAccBf, acc);
+            else
+              mma_ts(tmem + Cfg::kTAcc1, pa, dC1hMN + so + ko, kIdescAccH, acc);
+          }
+          if (parts & 2) {
+            if (kDkDv)   // dK += dS Q_i with dS in bf16 and Q_i as loaded
+              mma_ts(tmem + Cfg::kTAcc2, da, dC1MN + so + ko, kIdescAccBf, acc);
+            else
+              mma_ts(tmem + Cfg::kTAcc2, da, dC1hMN + so + ko, kIdescAccH, acc);
+          }
         }
         mma_commit(&bars->c_empty[cb % S]);
       }
@@ -398,8 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_c = [&](int cb) {
       return warp_wait(&bars->c_full[cb % S], (cb / S) & 1, abort_flag, kWaitBudget);
     };
-    auto wait_acc_inputs = [&](int cb, bool item_first, int li) {
-      bool ok = warp_wait(&bars->conv_full[cb % S], (cb / S) & 1, abort_flag, kWaitBudget);
+    // need_conv: the MMAs read the fp16 copy of the streamed C1 tile
+    auto wait_acc_inputs = [&](int cb, bool item_first, int li, bool need_conv = true) {
+      bool ok = !need_conv ||
+                warp_wait(&bars->conv_full[cb % S], (cb / S) & 1, abort_flag, kWaitBudget);
       // the first accumulation of an item overwrites the accumulators: the
       // previous item's epilogue must have read them
       if (ok && item_first && li > 0)
@@ -413,6 +432,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
       const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
+      if (kWide && warp == 2) {
+        // second MMA warp (wide layout): the acc2 accumulations of every
+        // block, concurrently with warp 1's acc1 ones (a single issuing
+        // thread cannot keep the tensor pipe busy with N = 64 MMAs)
+        for (int t = 0; t < w.nb; ++t) {
+          const int cb = c + t;
+          if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
+              !wait_acc_inputs(cb, t == 0, li, !kDkDv)) {
+            ok = false;
+            break;
+          }
+          ++npd;
+          tc_fence_after();
+          issue_acc(cb, t == 0, Cfg::kTP, Cfg::kTdS, 2);
+          mma_commit_w(&bars->acc_done, leader);
+          if (t == w.nb - 1) mma_commit_w(&bars->acc_full, leader);
+        }
+        c += w.nb;
+        continue;
+      }
       if (!warp_wait(&bars->r_full, li & 1, abort_flag, kWaitBudget)) {
         ok = false;
         break;
@@ -437,13 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_w(&bars->r_empty, leader);   // all S/dP of this item issued
           }
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
-              !wait_acc_inputs(cb, t == 0, li)) {
+              !wait_acc_inputs(cb, t == 0, li, !kDkDv)) {
             ok = false;
             break;
           }
           ++npd;
           tc_fence_after();
-          issue_acc(cb, t == 0, Cfg::kTP, Cfg::kTdS);
+          issue_acc(cb, t == 0, Cfg::kTP, Cfg::kTdS, 1);
           mma_commit_w(&bars->acc_done, leader);
           if (t == w.nb - 1) mma_commit_w(&bars->acc_full, leader);
         }
@@ -462,12 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t >= 1) {
             const int pb = cb - 1;
             if (!warp_wait(&bars->p_full[pb & 1], (pb >> 1) & 1, abort_flag, kWaitBudget) ||
-                !wait_acc_inputs(pb, t == 1, li)) {
+                !wait_acc_inputs(pb, t == 1, li, !kDkDv)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_acc(pb, t == 1, Cfg::kTS + (pb & 1) * kBlk, Cfg::kTdP + (pb & 1) * kBlk);
+            issue_acc(pb, t == 1, Cfg::kTS + (pb & 1) * kBlk, Cfg::kTdP + (pb & 1) * kBlk, 3);
             if (t == w.nb) mma_commit_w(&bars->acc_full, leader);
           }
         }
@@ -479,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(&bars->drain, 0, nullptr, kDrainBudget);
     __syncwarp();
   } else if (run && warp == 2) {
-    // ============ per-query L and D of each streamed block (dK/dV) ============
+    // ===== narrow layout: per-query L and D of each streamed block (dK/dV) =====
     if (kDkDv) {
       int c = 0, li = 0;
       bool ok = true;
@@ -517,17 +556,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (run && warp == 3) {
     // ============ fp16 copy of each streamed C1 tile (same swizzled layout) ============
+    // Wide layout, dK/dV kernel: first the per-query -L2 and -D of the block
+    // (read from global memory before the block has landed).
     constexpr int kVecs = Cfg::kBlkTile / 16;
+    constexpr bool kVec = kWide && kDkDv;
     int c = 0, li = 0;
     bool ok = true;
     for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
       const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
+      const size_t hb = (static_cast<size_t>(w.b) * H + w.h) * N;
       for (int t = 0; t < w.nb; ++t, ++c) {
         const int s = c % S;
+        float nl2[kBlk / 32], nd[kBlk / 32];
+        if constexpr (kVec) {
+#pragma unroll
+          for (int u = 0; u < kBlk / 32; ++u) {
+            const int q = (w.i0 + t) * kBlk + u * 32 + lane;
+            float l2 = INFINITY, dd = 0.0f;   // padded or fully masked query: P = 0
+            if (q < N) {
+              const float L = p.lse[hb + q];
+              if (L != -INFINITY) {
+                l2 = L * kLog2e;
+                dd = p.D[hb + q];
+              }
+            }
+            nl2[u] = -l2;   // stored negated: the exponent is s c + (-L2)
+            nd[u] = -dd;
+          }
+        }
         if (!warp_wait(&bars->c_full[s], (c / S) & 1, abort_flag, kWaitBudget)) {
           ok = false;
           break;
         }
+        if constexpr (kVec) {
+          float* vec = stage_vec(s);
+#pragma unroll
+          for (int u = 0; u < kBlk / 32; ++u) {
+            vec[u * 32 + lane] = nl2[u];
+            vec[kBlk + u * 32 + lane] = nd[u];
+          }
+          mbar_arrive(&bars->vec_full[s]);
+        }
+        if (kDkDv) continue;   // the dK/dV kernel's MMAs use the tiles as loaded
         const uint4* src = reinterpret_cast<const uint4*>(stage_c1(s));
         uint4* dst = reinterpret_cast<uint4*>(stage_c1h(s));
 #pragma unroll 4
@@ -545,7 +615,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) raise_abort(bars, p.status);
     __syncwarp();
-  } else if (run && warp >= 4) {
+  }
+  };
+  auto elementwise_role = [&]() {
+  if (run) {
     // ======================= element-wise warpgroups =======================
     const int g = (warp - 4) / 4;
     const int quarter = warp & 3;
@@ -628,35 +701,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Element-wise math on packed pairs (f32x2): t = s c - L2,
         // P = 2^t, dS = P (dP - D); the dQ kernel also sums P dP per row.
-        const float2* nl2v = kDkDv ? reinterpret_cast<const float2*>(stage_vec(s) + colg) : nullptr;
-        const float2* ndv = kDkDv ? reinterpret_cast<const float2*>(stage_vec(s) + kBlk + colg)
+        // dK/dV: the per-column -L2 and -D come from shared memory (the same
+        // values for every row), read 8 columns at a time with 16-byte loads
+        // one chunk ahead of their use, so the load latency overlaps the math.
+        const float4* nl2v = kDkDv ? reinterpret_cast<const float4*>(stage_vec(s) + colg) : nullptr;
+        const float4* ndv = kDkDv ? reinterpret_cast<const float4*>(stage_vec(s) + kBlk + colg)
                                   : nullptr;
         const uint64_t c2 = f2_pack(c, c);
         const uint64_t nl2_row = f2_pack(-l2_row, -l2_row);
         const uint64_t nd_row = f2_pack(-d_row, -d_row);
         uint64_t dacc2 = 0;   // (+0.0f, +0.0f)
         uint32_t pk[32], dk[32];
+        float4 vl[2], vd[2];   // the chunk being used
+        if (kDkDv) {
+          vl[0] = nl2v[0]; vl[1] = nl2v[1];
+          vd[0] = ndv[0]; vd[1] = ndv[1];
+        }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          uint64_t nl2, nd;
-          if (kDkDv) {
-            const float2 a = nl2v[i], bq = ndv[i];
-            nl2 = f2_pack(a.x, a.y);
-            nd = f2_pack(bq.x, bq.y);
-          } else {
-            nl2 = nl2_row;
-            nd = nd_row;
+        for (int ch = 0; ch < 8; ++ch) {   // 8 columns (4 pairs) per chunk
+          float4 nl[2], nn[2];
+          if (kDkDv && ch + 1 < 8) {
+            nl[0] = nl2v[2 * ch + 2]; nl[1] = nl2v[2 * ch + 3];
+            nn[0] = ndv[2 * ch + 2]; nn[1] = ndv[2 * ch + 3];
           }
-          const uint64_t s2 = f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
-          const uint64_t dp2 = f2_pack(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]));
-          const uint64_t t2 = f2_fma(s2, c2, nl2);
-          const float p0 = fast_exp2(f2_lo(t2));
-          const float p1 = fast_exp2(f2_hi(t2));
-          const uint64_t p2 = f2_pack(p0, p1);
-          if (!kDkDv) dacc2 = f2_fma(p2, dp2, dacc2);
-          const uint64_t ds2 = f2_mul(p2, f2_add(dp2, nd));
-          pk[i] = kDkDv ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
-          dk[i] = pack_f16x2(f2_lo(ds2), f2_hi(ds2));
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = ch * 4 + q;   // pair index: columns 2i, 2i+1
+            uint64_t nl2, nd;
+            if (kDkDv) {
+              const float4& a4 = vl[q >> 1];
+              const float4& d4 = vd[q >> 1];
+              nl2 = (q & 1) ? f2_pack(a4.z, a4.w) : f2_pack(a4.x, a4.y);
+              nd = (q & 1) ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y);
+            } else {
+              nl2 = nl2_row;
+              nd = nd_row;
+            }
+            const uint64_t s2 = f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+            const uint64_t dp2 = f2_pack(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]));
+            const uint64_t t2 = f2_fma(s2, c2, nl2);
+            const float p0 = fast_exp2(f2_lo(t2));
+            const float p1 = fast_exp2(f2_hi(t2));
+            const uint64_t p2 = f2_pack(p0, p1);
+            if (!kDkDv) dacc2 = f2_fma(p2, dp2, dacc2);
+            const uint64_t ds2 = f2_mul(p2, f2_add(dp2, nd));
+            pk[i] = kDkDv ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+            dk[i] = kDkDv ? pack_bf16x2(f2_lo(ds2), f2_hi(ds2)) : pack_f16x2(f2_lo(ds2), f2_hi(ds2));
+          }
+          if (kDkDv && ch + 1 < 8) {
+            vl[0] = nl[0]; vl[1] = nl[1];
+            vd[0] = nn[0]; vd[1] = nn[1];
+          }
         }
         if (!kDkDv) d_acc += f2_lo(dacc2) + f2_hi(dacc2);
         if (kWide) {
@@ -717,6 +812,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) raise_abort(bars, p.status);
     __syncwarp();
+  }
+  };
+  if (warp < 4) {
+    regs_dec<kRegsHelper>();
+    helper_roles();
+  } else {
+    regs_inc<kRegsElem>();
+    elementwise_role();
   }
 
   // ---- teardown ----
