@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->c_full[s], 1);
       mbar_init(&bars->c_empty[s], kWide ? 2 : 1);   // one commit per MMA warp
       mbar_init(&bars->vec_full[s], 32);
-      mbar_init(&bars->conv_full[s], 32);
+      mbar_init(&bars->conv_full[s], kWide ? 64 : 32);   // wide: warps 2 and 3 each convert half
     }
     mbar_init(&bars->sp_full, 1);
     mbar_init(&bars->sp_free, 256);
@@ -304,6 +304,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto stage_vec = [&](int s) {
     return reinterpret_cast<float*>(stage_c1(s) + 3 * Cfg::kBlkTile);
   };
+
+  // fp16 copy of part [v0, v1) (16-byte units) of stage s's C1 tile, same
+  // swizzled layout; the lanes of one warp share the range
+  auto convert_c1 = [&](int s, int v0, int v1) {
+    const uint4* src = reinterpret_cast<const uint4*>(stage_c1(s));
+    uint4* dst = reinterpret_cast<uint4*>(stage_c1h(s));
+#pragma unroll 4
+    for (int i = v0 + lane; i < v1; i += 32) {
+      uint4 v = src[i];
+      v.x = bf16x2_to_f16x2(v.x);
+      v.y = bf16x2_to_f16x2(v.y);
+      v.z = bf16x2_to_f16x2(v.z);
+      v.w = bf16x2_to_f16x2(v.w);
+      dst[i] = v;
+    }
+    fence_proxy_async_smem();   // make the copy visible to the tensor cores
+  };
+  constexpr int kVecs = Cfg::kBlkTile / 16;   // 16-byte units of a C1 tile
 
   // Role bodies; each runs inside the branch that sets its register budget
   // (setmaxnreg: the element-wise warps hold S, dP, P and dS of a row).
@@ -366,7 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dC1 = sdesc_sw128(smem_u32(stage_c1(0)), 16, 1024);
     const uint64_t dC2 = sdesc_sw128(smem_u32(stage_c2(0)), 16, 1024);
     const uint64_t dC1hMN = sdesc_sw128(smem_u32(stage_c1h(0)), Cfg::kBlkChunk, 1024);
-    const uint64_t dC1MN = sdesc_sw128(smem_u32(stage_c1(0)), Cfg::kBlkChunk, 1024);
     const uint64_t dC2MN = sdesc_sw128(smem_u32(stage_c2(0)), Cfg::kBlkChunk, 1024);
 
     // S and dP of global block cb into TMEM column offset `col`
@@ -401,12 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               mma_ts(tmem + Cfg::kTAcc1, pa, dC1hMN + so + ko, kIdescAccH, acc);
           }
-          if (parts & 2) {
-            if (kDkDv)   // dK += dS Q_i with dS in bf16 and Q_i as loaded
-              mma_ts(tmem + Cfg::kTAcc2, da, dC1MN + so + ko, kIdescAccBf, acc);
-            else
-              mma_ts(tmem + Cfg::kTAcc2, da, dC1hMN + so + ko, kIdescAccH, acc);
-          }
+          if (parts & 2) mma_ts(tmem + Cfg::kTAcc2, da, dC1hMN + so + ko, kIdescAccH, acc);
         }
         mma_commit(&bars->c_empty[cb % S]);
       }
@@ -438,8 +450,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // thread cannot keep the tensor pipe busy with N = 64 MMAs)
         for (int t = 0; t < w.nb; ++t) {
           const int cb = c + t;
+          // first half of the block's fp16 copy (warp 3 does the second)
+          if (!wait_c(cb)) {
+            ok = false;
+            break;
+          }
+          convert_c1(cb % S, 0, kVecs / 2);
+          mbar_arrive(&bars->conv_full[cb % S]);
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
-              !wait_acc_inputs(cb, t == 0, li, !kDkDv)) {
+              !wait_acc_inputs(cb, t == 0, li)) {
             ok = false;
             break;
           }
@@ -501,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t >= 1) {
             const int pb = cb - 1;
             if (!warp_wait(&bars->p_full[pb & 1], (pb >> 1) & 1, abort_flag, kWaitBudget) ||
-                !wait_acc_inputs(pb, t == 1, li, !kDkDv)) {
+                !wait_acc_inputs(pb, t == 1, li)) {
               ok = false;
               break;
             }
@@ -556,9 +575,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (run && warp == 3) {
     // ============ fp16 copy of each streamed C1 tile (same swizzled layout) ============
-    // Wide layout, dK/dV kernel: first the per-query -L2 and -D of the block
-    // (read from global memory before the block has landed).
-    constexpr int kVecs = Cfg::kBlkTile / 16;
+    // (wide layout: the second half; warp 2 converts the first).  Wide
+    // layout, dK/dV kernel: first the per-query -L2 and -D of the block (read
+    // from global memory before the block has landed).
     constexpr bool kVec = kWide && kDkDv;
     int c = 0, li = 0;
     bool ok = true;
@@ -597,19 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive(&bars->vec_full[s]);
         }
-        if (kDkDv) continue;   // the dK/dV kernel's MMAs use the tiles as loaded
-        const uint4* src = reinterpret_cast<const uint4*>(stage_c1(s));
-        uint4* dst = reinterpret_cast<uint4*>(stage_c1h(s));
-#pragma unroll 4
-        for (int i = lane; i < kVecs; i += 32) {
-          uint4 v = src[i];
-          v.x = bf16x2_to_f16x2(v.x);
-          v.y = bf16x2_to_f16x2(v.y);
-          v.z = bf16x2_to_f16x2(v.z);
-          v.w = bf16x2_to_f16x2(v.w);
-          dst[i] = v;
-        }
-        fence_proxy_async_smem();   // make the copy visible to the tensor cores
+        convert_c1(s, kWide ? kVecs / 2 : 0, kVecs);
         mbar_arrive(&bars->conv_full[s]);
       }
     }
@@ -746,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!kDkDv) dacc2 = f2_fma(p2, dp2, dacc2);
             const uint64_t ds2 = f2_mul(p2, f2_add(dp2, nd));
             pk[i] = kDkDv ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
-            dk[i] = kDkDv ? pack_bf16x2(f2_lo(ds2), f2_hi(ds2)) : pack_f16x2(f2_lo(ds2), f2_hi(ds2));
+            dk[i] = pack_f16x2(f2_lo(ds2), f2_hi(ds2));
           }
           if (kDkDv && ch + 1 < 8) {
             vl[0] = nl[0]; vl[1] = nl[1];
