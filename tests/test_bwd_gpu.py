@@ -112,6 +112,18 @@ def test_large_scores_backward_bf16():
         compare_bwd(inp, out, causal, default_scale(64), TOL["bf16"]["grad"])
 
 
+def test_large_scores_gradient_margin():
+    """64 heads of the BERT-shaped distribution (Q, K ~ N(0, 4^2), N = 512),
+    float32 gradients.  The staging precision of dS must keep the worst error
+    well inside the tolerance over many heads: rounding dS to bf16 alone
+    already reaches about 5e-2 on this distribution, fp16 staging about 5e-3."""
+    require_gpu()
+    inp = make(4, 16, 512, 64, "bf16", 9900, sigma={"q": 4.0, "k": 4.0})
+    out = run_fwd_bwd(inp, causal=False, grad_f32=True)
+    worst = compare_bwd(inp, out, False, default_scale(64), TOL["bf16"]["grad"])
+    assert all(e < 0.5 * TOL["bf16"]["grad"] for e in worst.values()), worst
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_workspace_d_matches_oracle(dtype):
     """After fa_bwd the workspace holds D = rowsum(dO * O), [B, H, N]: from the
