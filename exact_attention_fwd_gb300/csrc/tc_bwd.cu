@@ -94,12 +94,17 @@ struct BwdCfg {
   // stage: C1 (bf16) | C2 (bf16) | C1 as fp16 | vectors
   static constexpr int kStageBytes = 3 * kBlkTile + kVecBytes;
   static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
+  // row tiles (R1, R2) of an item; the wide layout double-buffers them so
+  // the next item's rows load while this item's last blocks run
+  static constexpr int kRBufs = kWide ? 2 : 1;
   static constexpr int kR1Off = 0;
   static constexpr int kR2Off = kRowTile;
-  static constexpr int kStageOff = 2 * kRowTile;
+  static constexpr int kRBufBytes = 2 * kRowTile;
+  static constexpr int kStageOff = kRBufs * kRBufBytes;
   static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
   static constexpr int kDsumOff = kBarOff + 512;         // 2 items x 2 warpgroups x 128
   static constexpr int kSmemBytes = kDsumOff + 2048 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per block");
   // TMEM columns
   static constexpr int kTS = 0;
   static constexpr int kTdP = 128;
@@ -111,7 +116,7 @@ struct BwdCfg {
 };
 
 struct BwdBars {
-  uint64_t r_full, r_empty;
+  uint64_t r_full[2], r_empty[2];
   uint64_t c_full[kStagesMax], c_empty[kStagesMax];
   uint64_t vec_full[kStagesMax], conv_full[kStagesMax];
   uint64_t sp_full, sp_free, pd_full, acc_done;   // wide layout
@@ -255,8 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- setup ----
   if (threadIdx.x == 0) {
-    mbar_init(&bars->r_full, 1);
-    mbar_init(&bars->r_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->r_full[b], 1);
+      mbar_init(&bars->r_empty[b], 1);
+    }
     for (int s = 0; s < S; ++s) {
       mbar_init(&bars->c_full[s], 1);
       mbar_init(&bars->c_empty[s], kWide ? 2 : 1);   // one commit per MMA warp
@@ -337,14 +344,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(li, num_items)) {
         const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
-        if (li > 0 && !mbar_wait(&bars->r_empty, (li - 1) & 1, abort_flag, kWaitBudget)) {
+        // row buffer rb, its use number ru
+        const int rb = li % Cfg::kRBufs, ru = li / Cfg::kRBufs;
+        if (ru > 0 &&
+            !mbar_wait(&bars->r_empty[rb], (ru - 1) & 1, abort_flag, kWaitBudget)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&bars->r_full, 2 * Cfg::kRowTile);
+        uint8_t* r1 = sR1 + rb * Cfg::kRBufBytes;
+        uint8_t* r2 = sR2 + rb * Cfg::kRBufBytes;
+        mbar_arrive_expect_tx(&bars->r_full[rb], 2 * Cfg::kRowTile);
         for (int ch = 0; ch < Cfg::kChunks; ++ch) {
-          tma_load_4d(sR1 + ch * Cfg::kRowChunk, &tmR1, &bars->r_full, ch * 64, w.h, w.row0, w.b);
-          tma_load_4d(sR2 + ch * Cfg::kRowChunk, &tmR2, &bars->r_full, ch * 64, w.h, w.row0, w.b);
+          tma_load_4d(r1 + ch * Cfg::kRowChunk, &tmR1, &bars->r_full[rb], ch * 64, w.h, w.row0,
+                      w.b);
+          tma_load_4d(r2 + ch * Cfg::kRowChunk, &tmR2, &bars->r_full[rb], ch * 64, w.h, w.row0,
+                      w.b);
         }
         ++li;
         for (int t = 0; t < w.nb; ++t) {
@@ -368,7 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) raise_abort(bars, p.status);
       for (int x = max(0, c - S); x < c; ++x)
         mbar_wait(&bars->c_full[x % S], (x / S) & 1, nullptr, kDrainBudget);
-      if (li > 0) mbar_wait(&bars->r_full, (li - 1) & 1, nullptr, kDrainBudget);
+      for (int x = max(0, li - Cfg::kRBufs); x < li; ++x)
+        mbar_wait(&bars->r_full[x % Cfg::kRBufs], (x / Cfg::kRBufs) & 1, nullptr, kDrainBudget);
     }
     __syncwarp();
   } else if (run && (warp == 1 || (kWide && warp == 2))) {
@@ -386,15 +401,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dC1hMN = sdesc_sw128(smem_u32(stage_c1h(0)), Cfg::kBlkChunk, 1024);
     const uint64_t dC2MN = sdesc_sw128(smem_u32(stage_c2(0)), Cfg::kBlkChunk, 1024);
 
-    // S and dP of global block cb into TMEM column offset `col`
-    auto issue_sp = [&](int cb, int col) {
+    // S and dP of global block cb into TMEM column offset `col`, rows from
+    // row buffer rb
+    auto issue_sp = [&](int cb, int col, int rb) {
       const uint64_t so = static_cast<uint64_t>(((cb % S) * Cfg::kStageBytes) >> 4);
+      const uint64_t rbo = static_cast<uint64_t>((rb * Cfg::kRBufBytes) >> 4);
       if (leader) {
         for (int kk = 0; kk < nks; ++kk) {
           const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * Cfg::kRowChunk + (kk & 3) * 32) >> 4);
           const uint64_t co = static_cast<uint64_t>(((kk >> 2) * Cfg::kBlkChunk + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + Cfg::kTS + col, dR1 + ro, dC1 + so + co, kIdescSP, kk > 0);
-          mma_ss(tmem + Cfg::kTdP + col, dR2 + ro, dC2 + so + co, kIdescSP, kk > 0);
+          mma_ss(tmem + Cfg::kTS + col, dR1 + rbo + ro, dC1 + so + co, kIdescSP, kk > 0);
+          mma_ss(tmem + Cfg::kTdP + col, dR2 + rbo + ro, dC2 + so + co, kIdescSP, kk > 0);
         }
       }
       __syncwarp();
@@ -471,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         c += w.nb;
         continue;
       }
-      if (!warp_wait(&bars->r_full, li & 1, abort_flag, kWaitBudget)) {
+      const int rb = li % Cfg::kRBufs;
+      if (!warp_wait(&bars->r_full[rb], (li / Cfg::kRBufs) & 1, abort_flag, kWaitBudget)) {
         ok = false;
         break;
       }
@@ -481,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (nsp > 0 && !warp_wait(&bars->sp_free, (nsp - 1) & 1, abort_flag, kWaitBudget))
             return false;
           tc_fence_after();
-          issue_sp(cb, 0);
+          issue_sp(cb, 0, rb);
           mma_commit_w(&bars->sp_full, leader);
           ++nsp;
           return true;
@@ -492,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t + 1 < w.nb) {
             if (!next_sp(cb + 1)) { ok = false; break; }
           } else {
-            mma_commit_w(&bars->r_empty, leader);   // all S/dP of this item issued
+            mma_commit_w(&bars->r_empty[rb], leader);   // all S/dP of this item issued
           }
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
               !wait_acc_inputs(cb, t == 0, li, !kDkDv)) {
@@ -513,9 +531,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t < w.nb) {
             if (!wait_c(cb)) { ok = false; break; }
             tc_fence_after();
-            issue_sp(cb, (cb & 1) * kBlk);
+            issue_sp(cb, (cb & 1) * kBlk, rb);
             mma_commit_w(&bars->s_full[cb & 1], leader);
-            if (t == w.nb - 1) mma_commit_w(&bars->r_empty, leader);
+            if (t == w.nb - 1) mma_commit_w(&bars->r_empty[rb], leader);
           }
           if (t >= 1) {
             const int pb = cb - 1;
