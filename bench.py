@@ -246,7 +246,10 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     dist = init_dist(world, True)
-    W = WORKLOAD
+    W = dict(WORKLOAD)
+    if args.batch:   # a smaller batch of the same shape, for profiler captures
+        W["B"] = args.batch
+        W["name"] = f"{W['name']}_b{args.batch}"
     B, H, N, d, causal = W["B"], W["H"], W["N"], W["d"], W["causal"]
     scale = 1.0 / math.sqrt(d)
     inp = Inputs(B, H, N, d, "bf16", W["seed"] + rank)
@@ -442,6 +445,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override B (profiler captures of a smaller case); 0 = the workload's")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
