@@ -693,6 +693,89 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        if constexpr (kDkDv && kWide) {
+          // dK/dV, wide layout: each thread takes 4 rows x 16 columns of the
+          // warpgroup's 64 (16x256b TMEM loads), so it needs the per-query
+          // -L2 and -D of 16 columns instead of 64.  Rows: lane group h
+          // (lanes 16h .. 16h+15 of the warp's quarter), rows t/4 and t/4+8
+          // of it; columns 8k + 2(t%4) and +1, k = 0..7.
+          uint32_t s4[2][32], d4[2][32];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld16x256_x8(tS + (static_cast<uint32_t>(16 * h) << 16), s4[h]);
+            tmem_ld16x256_x8(tdP + (static_cast<uint32_t>(16 * h) << 16), d4[h]);
+          }
+          tmem_ld_wait(s4[0]);
+          tmem_ld_wait(s4[1]);
+          tmem_ld_wait(d4[0]);
+          tmem_ld_wait(d4[1]);
+          tc_fence_before();
+          mbar_arrive(&bars->sp_free);
+          const int tq = lane & 3, tr = lane >> 2;
+          const int col0 = (w.i0 + t) * kBlk + colg;
+          // causal: query col0 + c is masked for key grow_r when c < grow_r - col0
+          if (kCausal && col0 < w.row0 + kRows - 1) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int lim = w.row0 + quarter * 32 + 16 * h + tr + 8 * e - col0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+#pragma unroll
+                  for (int b = 0; b < 2; ++b) {
+                    const int cidx = 8 * k + 2 * tq + b;
+                    uint32_t& v = s4[h][4 * k + 2 * e + b];
+                    v = (cidx < lim) ? __float_as_uint(-INFINITY) : v;
+                  }
+                }
+              }
+            }
+          }
+          const float* vbase = stage_vec(s) + colg + 2 * tq;
+          const uint64_t c2 = f2_pack(c, c);
+          uint32_t pk4[2][16], dk4[2][16];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float2 a = *reinterpret_cast<const float2*>(vbase + 8 * k);
+            const float2 bq = *reinterpret_cast<const float2*>(vbase + kBlk + 8 * k);
+            const uint64_t nl2 = f2_pack(a.x, a.y);
+            const uint64_t nd = f2_pack(bq.x, bq.y);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int ri = 4 * k + 2 * e;
+                const uint64_t s2 = f2_pack(__uint_as_float(s4[h][ri]), __uint_as_float(s4[h][ri + 1]));
+                const uint64_t dp2 = f2_pack(__uint_as_float(d4[h][ri]), __uint_as_float(d4[h][ri + 1]));
+                const uint64_t t2 = f2_fma(s2, c2, nl2);
+                const float p0 = fast_exp2(f2_lo(t2));
+                const float p1 = fast_exp2(f2_hi(t2));
+                const uint64_t ds2 = f2_mul(f2_pack(p0, p1), f2_add(dp2, nd));
+                pk4[h][2 * k + e] = pack_bf16x2(p0, p1);
+                dk4[h][2 * k + e] = pack_f16x2(f2_lo(ds2), f2_hi(ds2));
+              }
+            }
+          }
+          // P and dS columns are free once the previous block's accumulating
+          // MMAs have completed
+          if (nsp >= 2 &&
+              !warp_wait(&bars->acc_done, nsp & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          __syncwarp();   // tcgen05.st is warp-collective
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_st16x128_x8(tP + (static_cast<uint32_t>(16 * h) << 16), pk4[h]);
+            tmem_st16x128_x8(tdS + (static_cast<uint32_t>(16 * h) << 16), dk4[h]);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->pd_full);
+          continue;
+        }
         uint32_t sr[64], dr[64];
         tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
