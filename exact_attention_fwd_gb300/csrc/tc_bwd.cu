@@ -268,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->c_full[s], 1);
       mbar_init(&bars->c_empty[s], kWide ? 2 : 1);   // one commit per MMA warp
       mbar_init(&bars->vec_full[s], 32);
-      mbar_init(&bars->conv_full[s], kWide ? 64 : 32);   // wide: warps 2 and 3 each convert half
+      // wide layout: the 256 element-wise threads; narrow: warp 3
+      mbar_init(&bars->conv_full[s], kWide ? 256 : 32);
     }
     mbar_init(&bars->sp_full, 1);
     mbar_init(&bars->sp_free, 256);
@@ -314,11 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // fp16 copy of part [v0, v1) (16-byte units) of stage s's C1 tile, same
   // swizzled layout; the lanes of one warp share the range
-  auto convert_c1 = [&](int s, int v0, int v1) {
+  // (threads: tid = 0 .. nthr-1 share the range)
+  auto convert_c1 = [&](int s, int v0, int v1, int tid, int nthr) {
     const uint4* src = reinterpret_cast<const uint4*>(stage_c1(s));
     uint4* dst = reinterpret_cast<uint4*>(stage_c1h(s));
 #pragma unroll 4
-    for (int i = v0 + lane; i < v1; i += 32) {
+    for (int i = v0 + tid; i < v1; i += nthr) {
       uint4 v = src[i];
       v.x = bf16x2_to_f16x2(v.x);
       v.y = bf16x2_to_f16x2(v.y);
@@ -467,13 +469,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // thread cannot keep the tensor pipe busy with N = 64 MMAs)
         for (int t = 0; t < w.nb; ++t) {
           const int cb = c + t;
-          // first half of the block's fp16 copy (warp 3 does the second)
-          if (!wait_c(cb)) {
-            ok = false;
-            break;
-          }
-          convert_c1(cb % S, 0, kVecs / 2);
-          mbar_arrive(&bars->conv_full[cb % S]);
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
               !wait_acc_inputs(cb, t == 0, li)) {
             ok = false;
@@ -634,7 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive(&bars->vec_full[s]);
         }
-        convert_c1(s, kWide ? kVecs / 2 : 0, kVecs);
+        if (kWide) continue;   // the element-wise warps make the wide layout's copy
+        convert_c1(s, 0, kVecs, lane, 32);
         mbar_arrive(&bars->conv_full[s]);
       }
     }
@@ -705,6 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld16x256_x8(tS + (static_cast<uint32_t>(16 * h) << 16), s4[h]);
             tmem_ld16x256_x8(tdP + (static_cast<uint32_t>(16 * h) << 16), d4[h]);
           }
+          // while the loads are in flight: this block's fp16 copy of C1 for
+          // the dK accumulation (the block has landed: its S was computed)
+          convert_c1(s, 0, kVecs, threadIdx.x - 128, 256);
+          mbar_arrive(&bars->conv_full[s]);
           tmem_ld_wait(s4[0]);
           tmem_ld_wait(s4[1]);
           tmem_ld_wait(d4[0]);
@@ -781,6 +781,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_ld32(tdP, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
         tmem_ld32(tdP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+        if (kWide) {
+          // while the loads are in flight: this block's fp16 copy of C1
+          convert_c1(s, 0, kVecs, threadIdx.x - 128, 256);
+          mbar_arrive(&bars->conv_full[s]);
+        }
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
         if (kWide) {
