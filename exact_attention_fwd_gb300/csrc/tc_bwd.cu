@@ -268,8 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->c_full[s], 1);
       mbar_init(&bars->c_empty[s], kWide ? 2 : 1);   // one commit per MMA warp
       mbar_init(&bars->vec_full[s], 32);
-      // wide layout: the 256 element-wise threads; narrow: warp 3
-      mbar_init(&bars->conv_full[s], kWide ? 256 : 32);
+      // who makes the fp16 copy: dK/dV wide: the 256 element-wise threads;
+      // dQ wide: warps 2 and 3 (half each); narrow: warp 3
+      mbar_init(&bars->conv_full[s], kWide ? (kDkDv ? 256 : 64) : 32);
     }
     mbar_init(&bars->sp_full, 1);
     mbar_init(&bars->sp_free, 256);
@@ -469,6 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // thread cannot keep the tensor pipe busy with N = 64 MMAs)
         for (int t = 0; t < w.nb; ++t) {
           const int cb = c + t;
+          if (!kDkDv) {   // dQ: first half of the block's fp16 copy (warp 3 the second)
+            if (!wait_c(cb)) {
+              ok = false;
+              break;
+            }
+            convert_c1(cb % S, 0, kVecs / 2, lane, 32);
+            mbar_arrive(&bars->conv_full[cb % S]);
+          }
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
               !wait_acc_inputs(cb, t == 0, li)) {
             ok = false;
@@ -588,9 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (run && warp == 3) {
     // ============ fp16 copy of each streamed C1 tile (same swizzled layout) ============
-    // (wide layout: the second half; warp 2 converts the first).  Wide
-    // layout, dK/dV kernel: first the per-query -L2 and -D of the block (read
-    // from global memory before the block has landed).
+    // Narrow layout: the whole copy.  dQ, wide: the second half (warp 2 makes
+    // the first).  dK/dV, wide: no copy (the element-wise warps make it), but
+    // the per-query -L2 and -D of each block (read from global memory before
+    // the block has landed).
     constexpr bool kVec = kWide && kDkDv;
     int c = 0, li = 0;
     bool ok = true;
@@ -629,8 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive(&bars->vec_full[s]);
         }
-        if (kWide) continue;   // the element-wise warps make the wide layout's copy
-        convert_c1(s, 0, kVecs, lane, 32);
+        if (kWide && kDkDv) continue;   // the element-wise warps make this copy
+        convert_c1(s, kWide ? kVecs / 2 : 0, kVecs, lane, 32);
         mbar_arrive(&bars->conv_full[s]);
       }
     }
@@ -781,11 +791,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_ld32(tdP, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
         tmem_ld32(tdP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
-        if (kWide) {
-          // while the loads are in flight: this block's fp16 copy of C1
-          convert_c1(s, 0, kVecs, threadIdx.x - 128, 256);
-          mbar_arrive(&bars->conv_full[s]);
-        }
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
         if (kWide) {
