@@ -122,6 +122,7 @@ struct BwdBars {
   uint64_t sp_full, sp_free, pd_full, acc_done;   // wide layout
   uint64_t s_full[2], p_full[2];                  // narrow layout
   uint64_t acc_full, acc_free, dsum;
+  uint64_t epi_staged;   // wide layout, bf16 gradients: the staging tiles are written
   uint64_t drain, probe;
   uint32_t tmem_base;
   int abort;
@@ -233,6 +234,38 @@ __device__ __forceinline__ void store_acc_cols(uint32_t acc, uint32_t acc_b, flo
   }
 }
 
+// Same as store_acc_cols for bf16 output, but into a shared-memory staging
+// tile in the TMA box layout (rows of 128 bytes; 16-byte chunk c of row r at
+// chunk c ^ (r & 7)); the TMA store clips rows >= N and columns >= d.
+template <bool kCorr>
+__device__ __forceinline__ void stage_acc_cols(uint32_t acc, uint32_t acc_b, float corr, int col0,
+                                               int ncols, float mult, uint8_t* stage, int row) {
+  for (int cc = col0; cc < col0 + ncols; cc += 32) {
+    uint32_t r[32];
+    __syncwarp();   // tcgen05.ld is warp-collective
+    tmem_ld32(acc + cc, r);
+    tmem_ld_wait(r);
+    if (kCorr) {
+      uint32_t rb[32];
+      tmem_ld32(acc_b + cc, rb);
+      tmem_ld_wait(rb);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        r[i] = __float_as_uint(fmaf(corr, __uint_as_float(rb[i]), __uint_as_float(r[i])));
+    }
+#pragma unroll
+    for (int qv = 0; qv < 4; ++qv) {
+      const int chunk = (cc >> 3) + qv;   // 16-byte chunk (8 columns) of the row
+      uint4 v;
+      v.x = pack_bf16x2(__uint_as_float(r[qv * 8 + 0]) * mult, __uint_as_float(r[qv * 8 + 1]) * mult);
+      v.y = pack_bf16x2(__uint_as_float(r[qv * 8 + 2]) * mult, __uint_as_float(r[qv * 8 + 3]) * mult);
+      v.z = pack_bf16x2(__uint_as_float(r[qv * 8 + 4]) * mult, __uint_as_float(r[qv * 8 + 5]) * mult);
+      v.w = pack_bf16x2(__uint_as_float(r[qv * 8 + 6]) * mult, __uint_as_float(r[qv * 8 + 7]) * mult);
+      *reinterpret_cast<uint4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4)) = v;
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
   const float lo = __uint_as_float(x << 16);
   const float hi = __uint_as_float(x & 0xffff0000u);
@@ -243,6 +276,7 @@ template <int DP, bool kCausal, bool kDkDv, bool kF32Grad>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
                   const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmC2,
+                  const __grid_constant__ CUtensorMap tmG1, const __grid_constant__ CUtensorMap tmG2,
                   const BwdParams p) {
   using Cfg = BwdCfg<DP>;
   constexpr int S = Cfg::kStages;
@@ -283,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->acc_full, kWide ? 2 : 1);
     mbar_init(&bars->acc_free, 256);
     mbar_init(&bars->dsum, 256);
+    mbar_init(&bars->epi_staged, 256);
     mbar_init(&bars->drain, kWide ? 2 : 1);
     mbar_init(&bars->probe, 1);
     bars->abort = 0;
@@ -514,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t + 1 < w.nb) {
             if (!next_sp(cb + 1)) { ok = false; break; }
           } else {
-            mma_commit_w(&bars->r_empty[rb], leader);   // all S/dP of this item issued
+            // (wide layout: the epilogue releases the row buffer, which it
+            // uses as the staging tile of the gradient stores)
           }
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
               !wait_acc_inputs(cb, t == 0, li, !kDkDv)) {
@@ -915,20 +951,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         return kF32Grad ? static_cast<void*>(static_cast<float*>(base) + roff)
                         : static_cast<void*>(static_cast<__nv_bfloat16*>(base) + roff);
       };
-      if (kDkDv) {
-        store_acc_cols<kF32Grad, false>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg, half_cols,
-                                        1.0f, row_ptr(p.dv), p.d, store);
-        store_acc_cols<kF32Grad, false>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg, half_cols,
-                                        p.scale, row_ptr(p.dk), p.d, store);
+      if constexpr (kWide && !kF32Grad) {
+        // Wide layout, bf16 gradients: stage the rows in this item's row
+        // buffer (its last S/dP MMAs have completed, acc_full says so) and
+        // write them with TMA tensor stores; the buffer is released to the
+        // producer once the stores have read it.
+        const int rb = li % Cfg::kRBufs;
+        uint8_t* st1 = sR1 + rb * Cfg::kRBufBytes;
+        uint8_t* st2 = sR2 + rb * Cfg::kRBufBytes;
+        if (kDkDv) {
+          stage_acc_cols<false>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg, half_cols, 1.0f,
+                                st1, row);
+          stage_acc_cols<false>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg, half_cols, p.scale,
+                                st2, row);
+        } else {
+          stage_acc_cols<true>(tmem + lane_base + Cfg::kTAcc2, tmem + lane_base + Cfg::kTAcc1, corr,
+                               cbeg, half_cols, p.scale, st1, row);
+        }
+        fence_proxy_async_smem();   // the TMA engine reads what the threads wrote
+        tc_fence_before();
+        mbar_arrive(&bars->acc_free);
+        mbar_arrive(&bars->epi_staged);
+        if (threadIdx.x == 128) {
+          if (!mbar_wait(&bars->epi_staged, li & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+          } else {
+            tma_store_4d(&tmG1, st1, 0, w.h, w.row0, w.b);
+            if (kDkDv) tma_store_4d(&tmG2, st2, 0, w.h, w.row0, w.b);
+            bulk_commit_group();
+            bulk_wait_read_all();
+            mbar_arrive(&bars->r_empty[rb]);
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
       } else {
-        store_acc_cols<kF32Grad, true>(tmem + lane_base + Cfg::kTAcc2, tmem + lane_base + Cfg::kTAcc1,
-                                       corr, cbeg, half_cols, p.scale, row_ptr(p.dq), p.d, store);
+        if (kDkDv) {
+          store_acc_cols<kF32Grad, false>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg,
+                                          half_cols, 1.0f, row_ptr(p.dv), p.d, store);
+          store_acc_cols<kF32Grad, false>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg,
+                                          half_cols, p.scale, row_ptr(p.dk), p.d, store);
+        } else {
+          store_acc_cols<kF32Grad, true>(tmem + lane_base + Cfg::kTAcc2,
+                                         tmem + lane_base + Cfg::kTAcc1, corr, cbeg, half_cols,
+                                         p.scale, row_ptr(p.dq), p.d, store);
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->acc_free);
+        // wide layout, fp32 gradients: the row buffer is free (acc_full)
+        if (kWide && threadIdx.x == 128) mbar_arrive(&bars->r_empty[li % Cfg::kRBufs]);
       }
-      tc_fence_before();
-      mbar_arrive(&bars->acc_free);
       cbase += w.nb;
     }
     if (!ok) raise_abort(bars, p.status);
+    // the gradient stores must have completed before the CTA exits
+    if (kWide && !kF32Grad && threadIdx.x == 128) bulk_wait_all();
     __syncwarp();
   }
   };
@@ -959,7 +1038,7 @@ int sm_count() {
 template <int DP, bool kCausal, bool kDkDv, bool kF32>
 cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
   using Cfg = BwdCfg<DP>;
-  CUtensorMap m[4];
+  CUtensorMap m[6];
   // dQ:    rows are Q, dO (128-row boxes), blocks are K, V.
   // dK/dV: rows are K, V, blocks are Q, dO.
   const void* r1 = kDkDv ? p.k : p.q;
@@ -970,6 +1049,14 @@ cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
   if (e == cudaSuccess) e = make_bhnd_tmap(&m[1], r2, p.B, p.N, p.H, p.d, kRows, 64);
   if (e == cudaSuccess) e = make_bhnd_tmap(&m[2], c1, p.B, p.N, p.H, p.d, Cfg::kBlk, 64);
   if (e == cudaSuccess) e = make_bhnd_tmap(&m[3], c2, p.B, p.N, p.H, p.d, Cfg::kBlk, 64);
+  // gradient outputs (bf16 gradients in the wide layout are stored by TMA):
+  // dK/dV kernel: dV, dK; dQ kernel: dQ.  Unused otherwise (copies of m[0]).
+  m[4] = m[0];
+  m[5] = m[0];
+  if (e == cudaSuccess && Cfg::kWide && !kF32) {
+    e = make_bhnd_tmap(&m[4], kDkDv ? p.dv : p.dq, p.B, p.N, p.H, p.d, kRows, 64);
+    if (e == cudaSuccess && kDkDv) e = make_bhnd_tmap(&m[5], p.dk, p.B, p.N, p.H, p.d, kRows, 64);
+  }
   if (e != cudaSuccess) return e;
   auto kern = bwd_tc_kernel<DP, kCausal, kDkDv, kF32>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
@@ -980,7 +1067,7 @@ cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
   if (sms <= 0) return cudaErrorInvalidDevice;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   BwdParams pc = p;
-  void* args[] = {&m[0], &m[1], &m[2], &m[3], &pc};
+  void* args[] = {&m[0], &m[1], &m[2], &m[3], &m[4], &m[5], &pc};
   return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads), args,
                           Cfg::kSmemBytes, st);
 }
