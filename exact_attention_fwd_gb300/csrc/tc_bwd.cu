@@ -700,6 +700,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int colg = kWide ? g * 64 : 0;    // first block column this warpgroup handles
     int cbase = 0, li = 0;
     int nsp = 0;    // wide: sp_full phases consumed
+    // thread 128 (wide layout, bf16 gradients): the row buffer whose staged
+    // gradient rows are being stored; it goes back to the producer once the
+    // TMA stores have read it, checked a block later so nobody waits for it
+    int pend_rb = -1;
+    auto release_rows = [&]() {
+      if (pend_rb >= 0) {
+        bulk_wait_read_all();
+        mbar_arrive(&bars->r_empty[pend_rb]);
+        pend_rb = -1;
+      }
+    };
     bool ok = true;
     for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
       const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
@@ -803,6 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+          if (threadIdx.x == 128) release_rows();
           // P and dS columns are free once the previous block's accumulating
           // MMAs have completed
           if (nsp >= 2 &&
@@ -909,6 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!kDkDv) d_acc += f2_lo(dacc2) + f2_hi(dacc2);
         if (kWide) {
+          if (threadIdx.x == 128) release_rows();
           // P and dS columns are free once the previous block's accumulating
           // MMAs have completed
           if (nsp >= 2 &&
@@ -979,8 +992,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_store_4d(&tmG1, st1, 0, w.h, w.row0, w.b);
             if (kDkDv) tma_store_4d(&tmG2, st2, 0, w.h, w.row0, w.b);
             bulk_commit_group();
-            bulk_wait_read_all();
-            mbar_arrive(&bars->r_empty[rb]);
+            pend_rb = rb;   // released once the stores have read it (next block)
           }
         }
         if (!__all_sync(0xffffffffu, ok)) {
@@ -1007,7 +1019,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) raise_abort(bars, p.status);
     // the gradient stores must have completed before the CTA exits
-    if (kWide && !kF32Grad && threadIdx.x == 128) bulk_wait_all();
+    if (kWide && !kF32Grad && threadIdx.x == 128) {
+      release_rows();
+      bulk_wait_all();
+    }
     __syncwarp();
   }
   };
