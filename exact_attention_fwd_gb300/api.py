@@ -10,7 +10,8 @@ import torch
 
 from . import _lib
 
-_DTYPES = {torch.float32: _lib.FA_DTYPE_F32, torch.bfloat16: _lib.FA_DTYPE_BF16}
+_DTYPES = {torch.float32: _lib.FA_DTYPE_F32, torch.bfloat16: _lib.FA_DTYPE_BF16,
+           torch.float16: _lib.FA_DTYPE_F16}
 
 
 def _check(t, name, dtype=None):
@@ -28,7 +29,7 @@ def _stream_handle(stream):
 
 
 def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
-    """O, LSE = attention(q, k, v).  q, k, v: [B, N, H, d] float32 or bfloat16."""
+    """O, LSE = attention(q, k, v).  q, k, v: [B, N, H, d] float32, bfloat16 or float16."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         _check(t, name, q.dtype)
     if q.dtype not in _DTYPES:

@@ -8,6 +8,7 @@
 // 32 consecutive flattened rows and its lanes read consecutive 16-byte chunks
 // of them: every load instruction of the warp is one contiguous 512-byte span.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "fa_common.cuh"
 
@@ -17,8 +18,23 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRowsPerWarp = 32;
 
-__device__ __forceinline__ float dot_chunk(const uint4& a, const uint4& b, bool bf16) {
-  if (bf16) {
+// elt: 0 float32, 1 bf16, 2 fp16
+template <int kElt>
+__device__ __forceinline__ float dot_chunk(const uint4& a, const uint4& b) {
+  if (kElt == 2) {
+    const __half2* x = reinterpret_cast<const __half2*>(&a);
+    const __half2* y = reinterpret_cast<const __half2*>(&b);
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 fx = __half22float2(x[i]);
+      const float2 fy = __half22float2(y[i]);
+      s = fmaf(fx.x, fy.x, s);
+      s = fmaf(fx.y, fy.y, s);
+    }
+    return s;
+  }
+  if (kElt == 1) {
     const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
     const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
     float s = 0.0f;
@@ -39,12 +55,12 @@ __device__ __forceinline__ float dot_chunk(const uint4& a, const uint4& b, bool 
   return s;
 }
 
-template <bool kBf16>
+template <int kElt>
 __global__ void __launch_bounds__(kThreads) dot_do_o_kernel(BwdParams p) {
   // partial sums of one warp's rows: 32 rows x at most 32 chunks (fp32, d = 128)
   __shared__ float part[kThreads / 32][kRowsPerWarp * 32];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int elt = kBf16 ? 2 : 4;
+  const int elt = kElt ? 2 : 4;
   const int cpr = p.d * elt / 16;                       // 16-byte chunks per row
   const long long rows = static_cast<long long>(p.B) * p.N * p.H;
   const uint4* O = static_cast<const uint4*>(p.o);
@@ -60,7 +76,7 @@ __global__ void __launch_bounds__(kThreads) dot_do_o_kernel(BwdParams p) {
     for (int i = lane; i < nchunks; i += 32) {
       const uint4 a = __ldg(O + c0 + i);
       const uint4 b = __ldg(G + c0 + i);
-      part[warp][i] = dot_chunk(a, b, kBf16);
+      part[warp][i] = dot_chunk<kElt>(a, b);
     }
     __syncwarp();
     if (lane < nrows) {
@@ -80,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) dot_do_o_kernel(BwdParams p) {
 
 }  // namespace
 
-cudaError_t launch_bwd_dot(const BwdParams& p, bool bf16, cudaStream_t s) {
+cudaError_t launch_bwd_dot(const BwdParams& p, int elt, cudaStream_t s) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -91,8 +107,9 @@ cudaError_t launch_bwd_dot(const BwdParams& p, bool bf16, cudaStream_t s) {
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   void* args[] = {const_cast<BwdParams*>(&p)};
-  const void* kern = bf16 ? reinterpret_cast<const void*>(dot_do_o_kernel<true>)
-                          : reinterpret_cast<const void*>(dot_do_o_kernel<false>);
+  const void* kern = elt == 2   ? reinterpret_cast<const void*>(dot_do_o_kernel<2>)
+                     : elt == 1 ? reinterpret_cast<const void*>(dot_do_o_kernel<1>)
+                                : reinterpret_cast<const void*>(dot_do_o_kernel<0>);
   return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), args, 0, s);
 }
 

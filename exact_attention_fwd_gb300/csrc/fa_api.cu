@@ -88,8 +88,8 @@ size_t fa_bwd_workspace_size(int B, int H, int N) {
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, float scale, int causal, fa_dtype dtype, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (dtype == FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
-  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16)
+    return FA_ERR_INVALID_ARG;
   fa_status st = check_shape(B, H, N, d, scale);
   if (st != FA_OK) return st;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
@@ -114,9 +114,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.probe_timeout = probe_timeout_requested() ? 1 : 0;
+  p.f16 = (dtype == FA_DTYPE_F16) ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = (dtype == FA_DTYPE_F32) ? fa::launch_fwd_simt_f32(p, s, causal != 0)
-                                          : fa::launch_fwd_tc_bf16(p, s, causal != 0);
+                                          : fa::launch_fwd_tc16(p, s, causal != 0);
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -132,8 +133,8 @@ fa_status prepare_bwd(const void* q, const void* k, const void* v, const void* o
                       size_t workspace_bytes, fa::BwdParams* out) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
     return FA_ERR_INVALID_ARG;
-  if (dtype == FA_DTYPE_F16 || grad_dtype == FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
-  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16)
+    return FA_ERR_INVALID_ARG;
   if (grad_dtype != dtype && grad_dtype != FA_DTYPE_F32) return FA_ERR_INVALID_ARG;
   fa_status st = check_shape(B, H, N, d, scale);
   if (st != FA_OK) return st;
@@ -175,19 +176,19 @@ fa_status prepare_bwd(const void* q, const void* k, const void* v, const void* o
   p.grad_f32 = (grad_dtype == FA_DTYPE_F32) ? 1 : 0;
   p.status = status;
   p.probe_timeout = probe_timeout_requested() ? 1 : 0;
+  p.f16 = (dtype == FA_DTYPE_F16) ? 1 : 0;
   return FA_OK;
 }
 
 fa_status run_bwd_phase(const fa::BwdParams& p, int phase, fa_dtype dtype, bool causal,
                         cudaStream_t s) {
   cudaError_t e;
-  const bool bf16 = dtype == FA_DTYPE_BF16;
   if (phase == 0) {
-    e = fa::launch_bwd_dot(p, bf16, s);
-  } else if (!bf16) {
+    e = fa::launch_bwd_dot(p, dtype == FA_DTYPE_F32 ? 0 : (dtype == FA_DTYPE_BF16 ? 1 : 2), s);
+  } else if (dtype == FA_DTYPE_F32) {
     e = fa::launch_bwd_simt_f32(p, s, causal, phase);
   } else {
-    e = fa::launch_bwd_tc_bf16(p, s, causal, phase);
+    e = fa::launch_bwd_tc16(p, s, causal, phase);
   }
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

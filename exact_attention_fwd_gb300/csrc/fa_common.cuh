@@ -21,7 +21,7 @@ __device__ __forceinline__ void record_error(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
-// Forward launch parameters shared by the fp32 and bf16 paths.
+// Forward launch parameters shared by the fp32 and 16-bit paths.
 struct FwdParams {
   const void* q;
   const void* k;
@@ -33,6 +33,7 @@ struct FwdParams {
   float scale_log2;   // scale * log2(e)
   int* status;        // device status word
   int probe_timeout;  // nonzero: run the bounded-wait self-test and exit
+  int f16;            // 16-bit storage is fp16 (else bf16)
 };
 
 struct BwdParams {
@@ -52,16 +53,19 @@ struct BwdParams {
   int grad_f32;       // 1: gradients stored as float32
   int* status;
   int probe_timeout;
+  int f16;            // 16-bit storage (inputs, 16-bit gradients) is fp16 (else bf16)
 };
 
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_fwd_simt_f32(const FwdParams& p, cudaStream_t s, bool causal);
 cudaError_t launch_bwd_simt_f32(const BwdParams& p, cudaStream_t s, bool causal, int phase);
-cudaError_t launch_bwd_dot(const BwdParams& p, bool bf16, cudaStream_t s);
-// bf16 tensor-core path; returns cudaErrorNotSupported for shapes it does not
-// take.  Tensor maps are built inside from the raw pointers.
-cudaError_t launch_fwd_tc_bf16(const FwdParams& p, cudaStream_t s, bool causal);
+// elt: 0 float32, 1 bf16, 2 fp16 storage of O and dO
+cudaError_t launch_bwd_dot(const BwdParams& p, int elt, cudaStream_t s);
+// 16-bit (bf16 or fp16, p.f16) tensor-core path; returns
+// cudaErrorNotSupported for shapes it does not take.  Tensor maps are built
+// inside from the raw pointers.
+cudaError_t launch_fwd_tc16(const FwdParams& p, cudaStream_t s, bool causal);
 // phase 1: dQ kernel (also refines D in the workspace); phase 2: dK/dV kernel.
-cudaError_t launch_bwd_tc_bf16(const BwdParams& p, cudaStream_t s, bool causal, int phase);
+cudaError_t launch_bwd_tc16(const BwdParams& p, cudaStream_t s, bool causal, int phase);
 
 }  // namespace fa

@@ -344,6 +344,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Pack two floats as the kernels' 16-bit storage type: fp16 or bf16 (RNE).
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+  return kF16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+// Instruction descriptor for 16-bit A and B of that type.
+template <bool kF16>
+__host__ __device__ constexpr uint32_t idesc16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return kF16 ? idesc_f16(M, N, a_mn_major, b_mn_major) : idesc_bf16(M, N, a_mn_major, b_mn_major);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -180,7 +180,7 @@ __device__ __forceinline__ Item decode_item(int it, int N, int H) {
 // Store 32-column groups [col0, col0 + ncols) of this thread's accumulator row
 // at TMEM address `acc`, as mult * (acc + corr * acc_b) (acc_b read only when
 // kCorr), to a row of d elements of type float or bf16.
-template <bool kF32, bool kCorr>
+template <bool kF32, bool kCorr, bool kF16>
 __device__ __forceinline__ void store_acc_cols(uint32_t acc, uint32_t acc_b, float corr, int col0,
                                                int ncols, float mult, void* row_ptr, int d,
                                                bool store) {
@@ -219,13 +219,13 @@ __device__ __forceinline__ void store_acc_cols(uint32_t acc, uint32_t acc_b, flo
         const int col = cc + qv * 8;
         if (col < d) {
           uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(r[qv * 8 + 0]) * mult,
+          v.x = pack16x2<kF16>(__uint_as_float(r[qv * 8 + 0]) * mult,
                             __uint_as_float(r[qv * 8 + 1]) * mult);
-          v.y = pack_bf16x2(__uint_as_float(r[qv * 8 + 2]) * mult,
+          v.y = pack16x2<kF16>(__uint_as_float(r[qv * 8 + 2]) * mult,
                             __uint_as_float(r[qv * 8 + 3]) * mult);
-          v.z = pack_bf16x2(__uint_as_float(r[qv * 8 + 4]) * mult,
+          v.z = pack16x2<kF16>(__uint_as_float(r[qv * 8 + 4]) * mult,
                             __uint_as_float(r[qv * 8 + 5]) * mult);
-          v.w = pack_bf16x2(__uint_as_float(r[qv * 8 + 6]) * mult,
+          v.w = pack16x2<kF16>(__uint_as_float(r[qv * 8 + 6]) * mult,
                             __uint_as_float(r[qv * 8 + 7]) * mult);
           out[col / 8] = v;
         }
@@ -237,7 +237,7 @@ __device__ __forceinline__ void store_acc_cols(uint32_t acc, uint32_t acc_b, flo
 // Same as store_acc_cols for bf16 output, but into a shared-memory staging
 // tile in the TMA box layout (rows of 128 bytes; 16-byte chunk c of row r at
 // chunk c ^ (r & 7)); the TMA store clips rows >= N and columns >= d.
-template <bool kCorr>
+template <bool kCorr, bool kF16>
 __device__ __forceinline__ void stage_acc_cols(uint32_t acc, uint32_t acc_b, float corr, int col0,
                                                int ncols, float mult, uint8_t* stage, int row) {
   for (int cc = col0; cc < col0 + ncols; cc += 32) {
@@ -257,10 +257,10 @@ __device__ __forceinline__ void stage_acc_cols(uint32_t acc, uint32_t acc_b, flo
     for (int qv = 0; qv < 4; ++qv) {
       const int chunk = (cc >> 3) + qv;   // 16-byte chunk (8 columns) of the row
       uint4 v;
-      v.x = pack_bf16x2(__uint_as_float(r[qv * 8 + 0]) * mult, __uint_as_float(r[qv * 8 + 1]) * mult);
-      v.y = pack_bf16x2(__uint_as_float(r[qv * 8 + 2]) * mult, __uint_as_float(r[qv * 8 + 3]) * mult);
-      v.z = pack_bf16x2(__uint_as_float(r[qv * 8 + 4]) * mult, __uint_as_float(r[qv * 8 + 5]) * mult);
-      v.w = pack_bf16x2(__uint_as_float(r[qv * 8 + 6]) * mult, __uint_as_float(r[qv * 8 + 7]) * mult);
+      v.x = pack16x2<kF16>(__uint_as_float(r[qv * 8 + 0]) * mult, __uint_as_float(r[qv * 8 + 1]) * mult);
+      v.y = pack16x2<kF16>(__uint_as_float(r[qv * 8 + 2]) * mult, __uint_as_float(r[qv * 8 + 3]) * mult);
+      v.z = pack16x2<kF16>(__uint_as_float(r[qv * 8 + 4]) * mult, __uint_as_float(r[qv * 8 + 5]) * mult);
+      v.w = pack16x2<kF16>(__uint_as_float(r[qv * 8 + 6]) * mult, __uint_as_float(r[qv * 8 + 7]) * mult);
       *reinterpret_cast<uint4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4)) = v;
     }
   }
@@ -272,7 +272,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
   return pack_f16x2(lo, hi);
 }
 
-template <int DP, bool kCausal, bool kDkDv, bool kF32Grad>
+template <int DP, bool kCausal, bool kDkDv, bool kF32Grad, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
                   const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmC2,
@@ -427,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (run && (warp == 1 || (kWide && warp == 2))) {
     // ============ MMA issuers (whole warp waits, lane 0 issues) ============
     const uint32_t leader = (lane == 0) ? 1u : 0u;
-    constexpr uint32_t kIdescSP = idesc_bf16(kRows, kBlk, false, false);
-    constexpr uint32_t kIdescAccBf = idesc_bf16(kRows, DP, false, true);
+    constexpr uint32_t kIdescSP = idesc16<kF16>(kRows, kBlk, false, false);
+    constexpr uint32_t kIdescAccBf = idesc16<kF16>(kRows, DP, false, true);   // dV += P dO
     constexpr uint32_t kIdescAccH = idesc_f16(kRows, DP, false, true);
     const int nks = (p.d + 15) / 16;
     // descriptor bases; offsets advance the 16-byte start-address field
@@ -436,7 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dR2 = sdesc_sw128(smem_u32(sR2), 16, 1024);
     const uint64_t dC1 = sdesc_sw128(smem_u32(stage_c1(0)), 16, 1024);
     const uint64_t dC2 = sdesc_sw128(smem_u32(stage_c2(0)), 16, 1024);
-    const uint64_t dC1hMN = sdesc_sw128(smem_u32(stage_c1h(0)), Cfg::kBlkChunk, 1024);
+    // fp16 view of the streamed C1 tile: the copy, or (fp16 storage) the tile itself
+    const uint64_t dC1hMN = sdesc_sw128(smem_u32(kF16 ? stage_c1(0) : stage_c1h(0)),
+                                        Cfg::kBlkChunk, 1024);
     const uint64_t dC2MN = sdesc_sw128(smem_u32(stage_c2(0)), Cfg::kBlkChunk, 1024);
 
     // S and dP of global block cb into TMEM column offset `col`, rows from
@@ -484,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // need_conv: the MMAs read the fp16 copy of the streamed C1 tile
     auto wait_acc_inputs = [&](int cb, bool item_first, int li, bool need_conv = true) {
-      bool ok = !need_conv ||
+      bool ok = !need_conv || kF16 ||
                 warp_wait(&bars->conv_full[cb % S], (cb / S) & 1, abort_flag, kWaitBudget);
       // the first accumulation of an item overwrites the accumulators: the
       // previous item's epilogue must have read them
@@ -510,8 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            convert_c1(cb % S, 0, kVecs / 2, lane, 32);
-            mbar_arrive(&bars->conv_full[cb % S]);
+            if (!kF16) {
+              convert_c1(cb % S, 0, kVecs / 2, lane, 32);
+              mbar_arrive(&bars->conv_full[cb % S]);
+            }
           }
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
               !wait_acc_inputs(cb, t == 0, li)) {
@@ -676,6 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars->vec_full[s]);
         }
         if (kWide && kDkDv) continue;   // the element-wise warps make this copy
+        if (kF16) continue;   // fp16 storage: the tile itself is the operand
         convert_c1(s, kWide ? kVecs / 2 : 0, kVecs, lane, 32);
         mbar_arrive(&bars->conv_full[s]);
       }
@@ -760,8 +765,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // while the loads are in flight: this block's fp16 copy of C1 for
           // the dK accumulation (the block has landed: its S was computed)
-          convert_c1(s, 0, kVecs, threadIdx.x - 128, 256);
-          mbar_arrive(&bars->conv_full[s]);
+          if (!kF16) {
+            convert_c1(s, 0, kVecs, threadIdx.x - 128, 256);
+            mbar_arrive(&bars->conv_full[s]);
+          }
           tmem_ld_wait(s4[0]);
           tmem_ld_wait(s4[1]);
           tmem_ld_wait(d4[0]);
@@ -809,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float p0 = fast_exp2(f2_lo(t2));
                 const float p1 = fast_exp2(f2_hi(t2));
                 const uint64_t ds2 = f2_mul(f2_pack(p0, p1), f2_add(dp2, nd));
-                pk4[h][2 * k + e] = pack_bf16x2(p0, p1);
+                pk4[h][2 * k + e] = pack16x2<kF16>(p0, p1);
                 dk4[h][2 * k + e] = pack_f16x2(f2_lo(ds2), f2_hi(ds2));
               }
             }
@@ -911,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t p2 = f2_pack(p0, p1);
             if (!kDkDv) dacc2 = f2_fma(p2, dp2, dacc2);
             const uint64_t ds2 = f2_mul(p2, f2_add(dp2, nd));
-            pk[i] = kDkDv ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+            pk[i] = kDkDv ? pack16x2<kF16>(p0, p1) : pack_f16x2(p0, p1);
             dk[i] = pack_f16x2(f2_lo(ds2), f2_hi(ds2));
           }
           if (kDkDv && ch + 1 < 8) {
@@ -973,12 +980,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st1 = sR1 + rb * Cfg::kRBufBytes;
         uint8_t* st2 = sR2 + rb * Cfg::kRBufBytes;
         if (kDkDv) {
-          stage_acc_cols<false>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg, half_cols, 1.0f,
+          stage_acc_cols<false, kF16>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg, half_cols, 1.0f,
                                 st1, row);
-          stage_acc_cols<false>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg, half_cols, p.scale,
+          stage_acc_cols<false, kF16>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg, half_cols, p.scale,
                                 st2, row);
         } else {
-          stage_acc_cols<true>(tmem + lane_base + Cfg::kTAcc2, tmem + lane_base + Cfg::kTAcc1, corr,
+          stage_acc_cols<true, kF16>(tmem + lane_base + Cfg::kTAcc2, tmem + lane_base + Cfg::kTAcc1, corr,
                                cbeg, half_cols, p.scale, st1, row);
         }
         fence_proxy_async_smem();   // the TMA engine reads what the threads wrote
@@ -1001,12 +1008,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         if (kDkDv) {
-          store_acc_cols<kF32Grad, false>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg,
+          store_acc_cols<kF32Grad, false, kF16>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg,
                                           half_cols, 1.0f, row_ptr(p.dv), p.d, store);
-          store_acc_cols<kF32Grad, false>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg,
+          store_acc_cols<kF32Grad, false, kF16>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg,
                                           half_cols, p.scale, row_ptr(p.dk), p.d, store);
         } else {
-          store_acc_cols<kF32Grad, true>(tmem + lane_base + Cfg::kTAcc2,
+          store_acc_cols<kF32Grad, true, kF16>(tmem + lane_base + Cfg::kTAcc2,
                                          tmem + lane_base + Cfg::kTAcc1, corr, cbeg, half_cols,
                                          p.scale, row_ptr(p.dq), p.d, store);
         }
@@ -1050,7 +1057,7 @@ int sm_count() {
   return n;
 }
 
-template <int DP, bool kCausal, bool kDkDv, bool kF32>
+template <int DP, bool kCausal, bool kDkDv, bool kF32, bool kF16>
 cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
   using Cfg = BwdCfg<DP>;
   CUtensorMap m[6];
@@ -1060,20 +1067,21 @@ cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
   const void* r2 = kDkDv ? p.v : p.dO;
   const void* c1 = kDkDv ? p.q : p.k;
   const void* c2 = kDkDv ? p.dO : p.v;
-  cudaError_t e = make_bhnd_tmap(&m[0], r1, p.B, p.N, p.H, p.d, kRows, 64);
-  if (e == cudaSuccess) e = make_bhnd_tmap(&m[1], r2, p.B, p.N, p.H, p.d, kRows, 64);
-  if (e == cudaSuccess) e = make_bhnd_tmap(&m[2], c1, p.B, p.N, p.H, p.d, Cfg::kBlk, 64);
-  if (e == cudaSuccess) e = make_bhnd_tmap(&m[3], c2, p.B, p.N, p.H, p.d, Cfg::kBlk, 64);
+  cudaError_t e = make_bhnd_tmap(&m[0], r1, p.B, p.N, p.H, p.d, kRows, 64, kF16);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&m[1], r2, p.B, p.N, p.H, p.d, kRows, 64, kF16);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&m[2], c1, p.B, p.N, p.H, p.d, Cfg::kBlk, 64, kF16);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&m[3], c2, p.B, p.N, p.H, p.d, Cfg::kBlk, 64, kF16);
   // gradient outputs (bf16 gradients in the wide layout are stored by TMA):
   // dK/dV kernel: dV, dK; dQ kernel: dQ.  Unused otherwise (copies of m[0]).
   m[4] = m[0];
   m[5] = m[0];
   if (e == cudaSuccess && Cfg::kWide && !kF32) {
-    e = make_bhnd_tmap(&m[4], kDkDv ? p.dv : p.dq, p.B, p.N, p.H, p.d, kRows, 64);
-    if (e == cudaSuccess && kDkDv) e = make_bhnd_tmap(&m[5], p.dk, p.B, p.N, p.H, p.d, kRows, 64);
+    e = make_bhnd_tmap(&m[4], kDkDv ? p.dv : p.dq, p.B, p.N, p.H, p.d, kRows, 64, kF16);
+    if (e == cudaSuccess && kDkDv)
+      e = make_bhnd_tmap(&m[5], p.dk, p.B, p.N, p.H, p.d, kRows, 64, kF16);
   }
   if (e != cudaSuccess) return e;
-  auto kern = bwd_tc_kernel<DP, kCausal, kDkDv, kF32>;
+  auto kern = bwd_tc_kernel<DP, kCausal, kDkDv, kF32, kF16>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>((p.N + kRows - 1) / kRows) * p.B * p.H;
@@ -1091,8 +1099,11 @@ cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
 // kernel (phase 2) then reads, so the phases run in that order.
 template <int DP, bool kCausal, bool kF32>
 cudaError_t launch_phase(const BwdParams& p, cudaStream_t st, int phase) {
-  return phase == 1 ? launch_one<DP, kCausal, false, kF32>(p, st)
-                    : launch_one<DP, kCausal, true, kF32>(p, st);
+  if (p.f16)
+    return phase == 1 ? launch_one<DP, kCausal, false, kF32, true>(p, st)
+                      : launch_one<DP, kCausal, true, kF32, true>(p, st);
+  return phase == 1 ? launch_one<DP, kCausal, false, kF32, false>(p, st)
+                    : launch_one<DP, kCausal, true, kF32, false>(p, st);
 }
 
 template <int DP>
@@ -1105,7 +1116,7 @@ cudaError_t launch_dp(const BwdParams& p, cudaStream_t st, bool causal, int phas
 
 }  // namespace
 
-cudaError_t launch_bwd_tc_bf16(const BwdParams& p, cudaStream_t s, bool causal, int phase) {
+cudaError_t launch_bwd_tc16(const BwdParams& p, cudaStream_t s, bool causal, int phase) {
   if (phase != 1 && phase != 2) return cudaErrorInvalidValue;
   if (p.d <= 64) return launch_dp<64>(p, s, causal, phase);
   if (p.d <= 128) return launch_dp<128>(p, s, causal, phase);

@@ -164,7 +164,7 @@ __device__ __forceinline__ int item_index(int li, int num_items) {
   return it < num_items ? static_cast<int>(it) : -1;
 }
 
-template <int DP, bool kCausal>
+template <int DP, bool kCausal, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (instruction-descriptor bit 13, negate A), so the softmax always
       // works with a positive scale.
       const uint32_t kIdescQK =
-          idesc_bf16(kBM, kBN, false, false) | (p.scale_log2 < 0.0f ? (1u << 13) : 0u);
-      constexpr uint32_t kIdescPV = idesc_bf16(kBM, DP, false, true);
+          idesc16<kF16>(kBM, kBN, false, false) | (p.scale_log2 < 0.0f ? (1u << 13) : 0u);
+      constexpr uint32_t kIdescPV = idesc16<kF16>(kBM, DP, false, true);
       const int nks = (p.d + 15) / 16;       // K=16 steps over the head dim
       // Descriptor bases; K steps and stages advance the start-address field.
       const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p1 = fast_exp2(f2_hi(t));
             const uint64_t pp = f2_pack(p0, p1);
             if (i & 1) lsum1 = f2_add(lsum1, pp); else lsum0 = f2_add(lsum0, pp);
-            pk[i] = pack_bf16x2(p0, p1);
+            pk[i] = pack16x2<kF16>(p0, p1);
           }
           const uint64_t ls = f2_add(lsum0, lsum1);
           l += f2_lo(ls) + f2_hi(ls);
@@ -700,13 +700,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int qv = 0; qv < 4; ++qv) {
             const int chunk = cc * 4 + qv;   // 16-byte chunk of the row (8 columns)
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(orr[qv * 8 + 0]) * inv,
+            v.x = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 0]) * inv,
                               __uint_as_float(orr[qv * 8 + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(orr[qv * 8 + 2]) * inv,
+            v.y = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 2]) * inv,
                               __uint_as_float(orr[qv * 8 + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(orr[qv * 8 + 4]) * inv,
+            v.z = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 4]) * inv,
                               __uint_as_float(orr[qv * 8 + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(orr[qv * 8 + 6]) * inv,
+            v.w = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 6]) * inv,
                               __uint_as_float(orr[qv * 8 + 7]) * inv);
             *reinterpret_cast<uint4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4)) = v;
           }
@@ -741,13 +741,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int col = cc * 32 + qv * 8;
               if (col < p.d) {
                 uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(orr[qv * 8 + 0]) * inv,
+                v.x = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 0]) * inv,
                                   __uint_as_float(orr[qv * 8 + 1]) * inv);
-                v.y = pack_bf16x2(__uint_as_float(orr[qv * 8 + 2]) * inv,
+                v.y = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 2]) * inv,
                                   __uint_as_float(orr[qv * 8 + 3]) * inv);
-                v.z = pack_bf16x2(__uint_as_float(orr[qv * 8 + 4]) * inv,
+                v.z = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 4]) * inv,
                                   __uint_as_float(orr[qv * 8 + 5]) * inv);
-                v.w = pack_bf16x2(__uint_as_float(orr[qv * 8 + 6]) * inv,
+                v.w = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 6]) * inv,
                                   __uint_as_float(orr[qv * 8 + 7]) * inv);
                 orow[col / 8] = v;
               }
@@ -790,16 +790,16 @@ int sm_count() {
   return n;
 }
 
-template <int DP, bool kCausal>
+template <int DP, bool kCausal, bool kF16>
 cudaError_t launch_tc(const FwdParams& p, cudaStream_t st) {
   using Cfg = FwdCfg<DP>;
   CUtensorMap mq, mk, mv, mo;
-  cudaError_t e = make_bhnd_tmap(&mq, p.q, p.B, p.N, p.H, p.d);
-  if (e == cudaSuccess) e = make_bhnd_tmap(&mk, p.k, p.B, p.N, p.H, p.d);
-  if (e == cudaSuccess) e = make_bhnd_tmap(&mv, p.v, p.B, p.N, p.H, p.d);
-  if (e == cudaSuccess) e = make_bhnd_tmap(&mo, p.o, p.B, p.N, p.H, p.d);
+  cudaError_t e = make_bhnd_tmap(&mq, p.q, p.B, p.N, p.H, p.d, kBM, 64, kF16);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&mk, p.k, p.B, p.N, p.H, p.d, kBM, 64, kF16);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&mv, p.v, p.B, p.N, p.H, p.d, kBM, 64, kF16);
+  if (e == cudaSuccess) e = make_bhnd_tmap(&mo, p.o, p.B, p.N, p.H, p.d, kBM, 64, kF16);
   if (e != cudaSuccess) return e;
-  auto kern = fwd_tc_kernel<DP, kCausal>;
+  auto kern = fwd_tc_kernel<DP, kCausal, kF16>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nq = (p.N + kBM - 1) / kBM;
@@ -814,12 +814,18 @@ cudaError_t launch_tc(const FwdParams& p, cudaStream_t st) {
                           Cfg::kSmemBytes, st);
 }
 
+template <bool kF16>
+cudaError_t launch_dtype(const FwdParams& p, cudaStream_t s, bool causal) {
+  if (p.d <= 64) return causal ? launch_tc<64, true, kF16>(p, s) : launch_tc<64, false, kF16>(p, s);
+  if (p.d <= 128)
+    return causal ? launch_tc<128, true, kF16>(p, s) : launch_tc<128, false, kF16>(p, s);
+  return cudaErrorNotSupported;
+}
+
 }  // namespace
 
-cudaError_t launch_fwd_tc_bf16(const FwdParams& p, cudaStream_t s, bool causal) {
-  if (p.d <= 64) return causal ? launch_tc<64, true>(p, s) : launch_tc<64, false>(p, s);
-  if (p.d <= 128) return causal ? launch_tc<128, true>(p, s) : launch_tc<128, false>(p, s);
-  return cudaErrorNotSupported;
+cudaError_t launch_fwd_tc16(const FwdParams& p, cudaStream_t s, bool causal) {
+  return p.f16 ? launch_dtype<true>(p, s, causal) : launch_dtype<false>(p, s, causal);
 }
 
 }  // namespace fa

@@ -1,4 +1,4 @@
-// tmap.h — host-side TMA tensor-map encoding for [B, N, H, d] bf16 tensors.
+// tmap.h — host-side TMA tensor-map encoding for [B, N, H, d] bf16 or fp16 tensors.
 //
 // The map views a [B, N, H, d] tensor as 4-D with dims (d, H, N, B) and byte
 // strides (2, 2d, 2Hd, 2NHd).  The box is 64 x 1 x 128 x 1: 128 rows (tokens)
@@ -33,7 +33,7 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
 
 // rows_box: tokens per box (128); cols_box: head-dim columns per box (64).
 inline cudaError_t make_bhnd_tmap(CUtensorMap* map, const void* base, int B, int N, int H, int d,
-                                  int rows_box = 128, int cols_box = 64) {
+                                  int rows_box = 128, int cols_box = 64, bool f16 = false) {
   auto fn = encode_tiled_fn();
   if (fn == nullptr) return cudaErrorSymbolNotFound;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
@@ -44,7 +44,8 @@ inline cudaError_t make_bhnd_tmap(CUtensorMap* map, const void* base, int B, int
   const cuuint32_t box[4] = {static_cast<cuuint32_t>(cols_box), 1u,
                              static_cast<cuuint32_t>(rows_box), 1u};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+  const CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        4, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -43,7 +43,7 @@ typedef enum {
 typedef enum {
   FA_DTYPE_F32 = 0,   /* float32 storage, float32 arithmetic (SIMT path) */
   FA_DTYPE_BF16 = 1,  /* bf16 storage, fp32 accumulation (tcgen05 path) */
-  FA_DTYPE_F16 = 2    /* reserved; returns FA_ERR_UNSUPPORTED */
+  FA_DTYPE_F16 = 2    /* fp16 storage, fp32 accumulation (tcgen05 path); |values| < 65504 */
 } fa_dtype;
 
 /*
@@ -98,10 +98,11 @@ size_t fa_bwd_workspace_size(int B, int H, int N);
  *   other arguments as in fa_fwd.
  * Rows whose lse is -inf (no visible key) contribute nothing.
  *
- * bf16 path: D is first taken from the bf16 O as above, then refined in the
- * dQ kernel to the fp32 sum_j P_ij dP_ij (the same quantity without O's
- * storage rounding), and dQ is corrected accordingly; dS is staged for the
- * tensor cores in fp16, so |Q|, |K| and |dS| must stay below 65504.
+ * 16-bit paths (bf16, fp16): D is first taken from the 16-bit O as above,
+ * then refined in the dQ kernel to the fp32 sum_j P_ij dP_ij (the same
+ * quantity without O's storage rounding), and dQ is corrected accordingly;
+ * dS is staged for the tensor cores in fp16, so |Q|, |K| and |dS| must stay
+ * below 65504 (fp16 storage: every input and output too).
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  const float* lse, const void* dO,
@@ -117,8 +118,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
  *   0: the D pre-pass, D = rowsum(dO * O) into the workspace
  *      ("Flash Attention 2 — backward pass notes", option 1 of "Why the WGSL
  *      kernel isn't shipped this turn");
- *   1: the kernel that owns Q tiles and writes dQ (bf16 path: also refines D
- *      in the workspace);
+ *   1: the kernel that owns Q tiles and writes dQ (16-bit paths: also
+ *      refines D in the workspace);
  *   2: the kernel that owns K tiles and writes dK and dV (option 3).
  * Arguments, validation and errors as fa_bwd; phase outside [0, 2] returns
  * FA_ERR_INVALID_ARG.

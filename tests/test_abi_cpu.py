@@ -54,7 +54,7 @@ FAKE = 1 << 20   # 16-byte aligned address; validation fails before any use
     (dict(d=12), 1), (dict(d=0), 1),       # not a multiple of 8
     (dict(d=136), 2),                      # above 128
     (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
-    (dict(dtype=2), 2),                    # fp16 reserved
+    (dict(dtype=2, q=FAKE + 8), 1),        # fp16, misaligned
     (dict(dtype=7), 1),
     (dict(q=FAKE + 8), 1),                 # misaligned
     (dict(o=FAKE), 1),                     # output aliases q
@@ -71,6 +71,8 @@ def test_fwd_rejects_invalid_arguments(lib, kw, want):
     (dict(workspace=0), 1),
     (dict(workspace_bytes=100), 1),
     (dict(grad_dtype=1, dtype=0), 1),      # bf16 grads of fp32 inputs
+    (dict(grad_dtype=2, dtype=1), 1),      # fp16 grads of bf16 inputs
+    (dict(dtype=3, grad_dtype=3), 1),      # no such element type
     (dict(dq=FAKE), 1),                    # aliases q
     (dict(dk=8 * FAKE), 1),                # aliases dq
     (dict(workspace=FAKE + 16), 1),        # not 256-byte aligned (and aliases)
