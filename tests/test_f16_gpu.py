@@ -67,3 +67,17 @@ def test_causal_first_row_equals_v0_f16():
     o, lse, (q, k, v) = run_fwd(inp, causal=True)
     assert o.dtype == torch.float16
     assert torch.equal(o[:, 0], v[:, 0])
+
+
+def test_scores_beyond_fp16_exp_range():
+    """Scaled scores up to ~30, past ln 65520 = 11.09 where a naive fp16
+    exponential overflows (the facts page's "overflow" entry): the kernel
+    subtracts the running max in fp32 before exponentiating, so O and L stay
+    finite and match the oracle."""
+    torch = require_gpu()
+    inp = make(1, 2, 192, 64, "f16", 12200)
+    for causal in (False, True):
+        o, lse, _ = run_fwd(inp, causal=causal, scale=1.0)
+        assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+        assert float(lse.max()) > 11.0901
+        compare_fwd(inp, o, lse, causal, 1.0)
