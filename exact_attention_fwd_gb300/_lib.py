@@ -15,7 +15,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = ran
 FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F16 = range(3)
 
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_phase", "fa_bwd_workspace_size", "fa_sync_status",
-           "fa_status_string", "fa_bwd_noalloc")
+           "fa_status_string", "fa_bwd_noalloc", "fa_fwd_partial", "fa_merge",
+           "fa_fwd_splitkv_keys_per_split", "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv")
 FA_BWD_NOALLOC_MAX_ROWS = 1 << 22
 
 _lib = None
@@ -49,6 +50,16 @@ def load():
     lib.fa_bwd_workspace_size.restype = sz
     lib.fa_sync_status.argtypes = [vp]
     lib.fa_sync_status.restype = i
+    lib.fa_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp]
+    lib.fa_fwd_partial.restype = i
+    lib.fa_merge.argtypes = [vp, vp, i, i, i, vp, vp, i, i, i, i, i, vp]
+    lib.fa_merge.restype = i
+    lib.fa_fwd_splitkv_keys_per_split.argtypes = [i, i]
+    lib.fa_fwd_splitkv_keys_per_split.restype = i
+    lib.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_splitkv_workspace_size.restype = sz
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp, sz, vp]
+    lib.fa_fwd_splitkv.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -91,3 +102,29 @@ def fa_bwd_workspace_size(B, H, N):
 
 def fa_sync_status(stream):
     return load().fa_sync_status(stream)
+
+
+def fa_fwd_partial(q, k, v, o_part, lse_part, B, H, N, d, scale, causal, dtype, keys_per_split,
+                   stream):
+    return load().fa_fwd_partial(q, k, v, o_part, lse_part, B, H, N, d, float(scale),
+                                 int(causal), int(dtype), int(keys_per_split), stream)
+
+
+def fa_merge(o_part, lse_part, num_splits, keys_per_split, causal, o, lse, B, H, N, d, dtype,
+             stream):
+    return load().fa_merge(o_part, lse_part, int(num_splits), int(keys_per_split), int(causal),
+                           o, lse, B, H, N, d, int(dtype), stream)
+
+
+def fa_fwd_splitkv_keys_per_split(N, num_splits):
+    return int(load().fa_fwd_splitkv_keys_per_split(N, num_splits))
+
+
+def fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits):
+    return int(load().fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, num_splits, workspace,
+                   workspace_bytes, stream):
+    return load().fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, float(scale), int(causal),
+                                 int(dtype), int(num_splits), workspace, workspace_bytes, stream)

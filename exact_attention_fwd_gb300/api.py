@@ -86,6 +86,95 @@ def backward(q, k, v, o, lse, do, scale=None, causal=False, grad_dtype=None, ws=
     return dq, dk, dv
 
 
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, q.dtype)
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise ValueError("q, k, v must share one [B, N, H, d] shape")
+
+
+def forward_partial(q, k, v, keys_per_split, scale=None, causal=False, o_part=None,
+                    lse_part=None, stream=None):
+    """Attention of every row over each key slice alone (fa_fwd_partial).
+
+    Returns (o_part [S, B, N, H, d] float32, lse_part [S, B, H, N] float32),
+    S = ceil(N / keys_per_split); entries of slices a row does not read (causal:
+    slices that start after the row) are left as they were.
+    """
+    _check_qkv(q, k, v)
+    B, N, H, d = q.shape
+    S = -(-N // keys_per_split)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if o_part is None:
+        o_part = torch.empty((S, B, N, H, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((S, B, H, N), dtype=torch.float32, device=q.device)
+    _check(o_part, "o_part", torch.float32)
+    _check(lse_part, "lse_part", torch.float32)
+    st = _lib.fa_fwd_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_part.data_ptr(),
+                             lse_part.data_ptr(), B, H, N, d, scale, causal, _DTYPES[q.dtype],
+                             keys_per_split, _stream_handle(stream))
+    if st != _lib.FA_OK:
+        raise _lib.FaError(st, "fa_fwd_partial")
+    return o_part, lse_part
+
+
+def merge(o_part, lse_part, keys_per_split, causal=False, dtype=torch.bfloat16, out=None,
+          lse=None, stream=None):
+    """Merge per-slice results into (O [B, N, H, d] of `dtype`, LSE [B, H, N]) (fa_merge)."""
+    _check(o_part, "o_part", torch.float32)
+    _check(lse_part, "lse_part", torch.float32)
+    if o_part.dim() != 5:
+        raise ValueError("o_part must be [S, B, N, H, d]")
+    S, B, N, H, d = o_part.shape
+    if tuple(lse_part.shape) != (S, B, H, N):
+        raise ValueError("lse_part must be [S, B, H, N]")
+    if dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=dtype, device=o_part.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=o_part.device)
+    _check(out, "out", dtype)
+    _check(lse, "lse", torch.float32)
+    st = _lib.fa_merge(o_part.data_ptr(), lse_part.data_ptr(), S, keys_per_split, causal,
+                       out.data_ptr(), lse.data_ptr(), B, H, N, d, _DTYPES[dtype],
+                       _stream_handle(stream))
+    if st != _lib.FA_OK:
+        raise _lib.FaError(st, "fa_merge")
+    return out, lse
+
+
+def splitkv_workspace(B, H, N, d, num_splits, device):
+    """A device workspace tensor sized for fa_fwd_splitkv."""
+    n = _lib.fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def forward_splitkv(q, k, v, num_splits, scale=None, causal=False, out=None, lse=None, ws=None,
+                    stream=None):
+    """O, LSE = attention(q, k, v) as key slices then a merge (fa_fwd_splitkv)."""
+    _check_qkv(q, k, v)
+    B, N, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = splitkv_workspace(B, H, N, d, num_splits, q.device)
+    _check(out, "out", q.dtype)
+    _check(lse, "lse", torch.float32)
+    st = _lib.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr(), B, H, N, d, scale, causal, _DTYPES[q.dtype],
+                             num_splits, ws.data_ptr(), ws.numel(), _stream_handle(stream))
+    if st != _lib.FA_OK:
+        raise _lib.FaError(st, "fa_fwd_splitkv")
+    return out, lse
+
+
 def sync_status(stream=None):
     """Synchronise and return (and clear) the device status word."""
     return _lib.fa_sync_status(_stream_handle(stream))

@@ -237,3 +237,159 @@ fa_status fa_sync_status(void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// split-KV forward
+// ---------------------------------------------------------------------------
+
+namespace {
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t part_o_bytes(int B, int H, int N, int d, int nsplit) {
+  return static_cast<size_t>(nsplit) * B * N * H * d * sizeof(float);
+}
+size_t part_l_bytes(int B, int H, int N, int nsplit) {
+  return static_cast<size_t>(nsplit) * B * H * N * sizeof(float);
+}
+
+int slices_of(int N, int keys_per_split) { return (N + keys_per_split - 1) / keys_per_split; }
+
+fa_status run_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                      int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                      int keys_per_split, cudaStream_t s) {
+  int* status = nullptr;
+  fa_status err = FA_OK;
+  status = status_word(&err);
+  if (status == nullptr) return err;
+  fa::FwdParams p{};
+  p.q = q; p.k = k; p.v = v; p.o = nullptr; p.lse = nullptr;
+  p.B = B; p.H = H; p.N = N; p.d = d;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status;
+  p.probe_timeout = probe_timeout_requested() ? 1 : 0;
+  p.f16 = (dtype == FA_DTYPE_F16) ? 1 : 0;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.split_blocks = keys_per_split / 128;
+  p.nsplit = slices_of(N, keys_per_split);
+  cudaError_t e = fa::launch_fwd_tc16_partial(p, s, causal != 0);
+  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status run_merge(const float* o_part, const float* lse_part, int nsplit, int keys_per_split,
+                    int causal, void* o, float* lse, int B, int H, int N, int d, fa_dtype dtype,
+                    cudaStream_t s) {
+  fa::MergeParams m{};
+  m.o_part = o_part; m.lse_part = lse_part; m.o = o; m.lse = lse;
+  m.B = B; m.H = H; m.N = N; m.d = d;
+  m.nsplit = nsplit;
+  m.keys_per_split = keys_per_split;
+  m.causal = causal != 0;
+  const int elt = dtype == FA_DTYPE_F32 ? 0 : (dtype == FA_DTYPE_BF16 ? 1 : 2);
+  return fa::launch_merge(m, elt, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_splitkv_keys_per_split(int N, int num_splits) {
+  if (N < 1 || num_splits < 1) return 0;
+  const long long per = (static_cast<long long>(N) + 256LL * num_splits - 1) / (256LL * num_splits);
+  return static_cast<int>(256 * per);
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
+  if (B < 1 || H < 1 || N < 1 || d < 1 || num_splits < 1) return 0;
+  const int ns = slices_of(N, fa_fwd_splitkv_keys_per_split(N, num_splits));
+  return round256(part_o_bytes(B, H, N, d, ns)) + round256(part_l_bytes(B, H, N, ns));
+}
+
+fa_status fa_fwd_partial(const void* q, const void* k, const void* v, float* o_part,
+                         float* lse_part, int B, int H, int N, int d, float scale, int causal,
+                         fa_dtype dtype, int keys_per_split, void* stream) {
+  if (!q || !k || !v || !o_part || !lse_part) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16)
+    return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (keys_per_split < 256 || keys_per_split % 256 != 0) return FA_ERR_INVALID_ARG;
+  if (dtype == FA_DTYPE_F32) return FA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o_part, 16) ||
+      !aligned(lse_part, 4))
+    return FA_ERR_INVALID_ARG;
+  const int ns = slices_of(N, keys_per_split);
+  const size_t tbytes = static_cast<size_t>(B) * N * H * d * elt_size(dtype);
+  const size_t ob = part_o_bytes(B, H, N, d, ns), lb = part_l_bytes(B, H, N, ns);
+  if (static_cast<long double>(ob) >= static_cast<long double>(1ULL << 40)) return FA_ERR_UNSUPPORTED;
+  for (const void* in : {q, k, v})
+    if (overlaps(o_part, ob, in, tbytes) || overlaps(lse_part, lb, in, tbytes))
+      return FA_ERR_INVALID_ARG;
+  if (overlaps(o_part, ob, lse_part, lb)) return FA_ERR_INVALID_ARG;
+  return run_partial(q, k, v, o_part, lse_part, B, H, N, d, scale, causal, dtype, keys_per_split,
+                     static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_merge(const float* o_part, const float* lse_part, int num_splits, int keys_per_split,
+                   int causal, void* o, float* lse, int B, int H, int N, int d, fa_dtype dtype,
+                   void* stream) {
+  if (!o_part || !lse_part || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16)
+    return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d, 1.0f);
+  if (st != FA_OK) return st;
+  if (num_splits < 1 || keys_per_split < 1) return FA_ERR_INVALID_ARG;
+  if (!aligned(o_part, 16) || !aligned(o, 16) || !aligned(lse_part, 4) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  const size_t ob = part_o_bytes(B, H, N, d, num_splits), lb = part_l_bytes(B, H, N, num_splits);
+  if (static_cast<long double>(ob) >= static_cast<long double>(1ULL << 40)) return FA_ERR_UNSUPPORTED;
+  const size_t tbytes = static_cast<size_t>(B) * N * H * d * elt_size(dtype);
+  const size_t l1 = static_cast<size_t>(B) * H * N * sizeof(float);
+  if (overlaps(o, tbytes, o_part, ob) || overlaps(o, tbytes, lse_part, lb) ||
+      overlaps(lse, l1, o_part, ob) || overlaps(lse, l1, lse_part, lb) ||
+      overlaps(o, tbytes, lse, l1))
+    return FA_ERR_INVALID_ARG;
+  return run_merge(o_part, lse_part, num_splits, keys_per_split, causal, o, lse, B, H, N, d, dtype,
+                   static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                         int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16)
+    return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (num_splits < 1) return FA_ERR_INVALID_ARG;
+  if (dtype == FA_DTYPE_F32) return FA_ERR_UNSUPPORTED;
+  const size_t need = fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits);
+  if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return FA_ERR_INVALID_ARG;
+  const size_t tbytes = static_cast<size_t>(B) * N * H * d * elt_size(dtype);
+  const size_t lbytes = static_cast<size_t>(B) * H * N * sizeof(float);
+  for (const void* in : {q, k, v}) {
+    if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes) ||
+        overlaps(workspace, workspace_bytes, in, tbytes))
+      return FA_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, tbytes, lse, lbytes) || overlaps(workspace, workspace_bytes, o, tbytes) ||
+      overlaps(workspace, workspace_bytes, lse, lbytes))
+    return FA_ERR_INVALID_ARG;
+  const int kps = fa_fwd_splitkv_keys_per_split(N, num_splits);
+  const int ns = slices_of(N, kps);
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             round256(part_o_bytes(B, H, N, d, ns)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = run_partial(q, k, v, o_part, lse_part, B, H, N, d, scale, causal, dtype, kps, s);
+  if (st != FA_OK) return st;
+  return run_merge(o_part, lse_part, ns, kps, causal, o, lse, B, H, N, d, dtype, s);
+}
+
+}  // extern "C"

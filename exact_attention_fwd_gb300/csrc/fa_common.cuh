@@ -34,6 +34,23 @@ struct FwdParams {
   int* status;        // device status word
   int probe_timeout;  // nonzero: run the bounded-wait self-test and exit
   int f16;            // 16-bit storage is fp16 (else bf16)
+  // split-KV partial pass (launch_fwd_tc16_partial); unused otherwise
+  float* o_part;      // [nsplit, B, N, H, d] float32
+  float* lse_part;    // [nsplit, B, H, N] float32
+  int split_blocks;   // 128-key blocks per key slice (even)
+  int nsplit;         // key slices: ceil(N / (128 split_blocks))
+};
+
+// fa_merge's launch parameters.
+struct MergeParams {
+  const float* o_part;
+  const float* lse_part;
+  void* o;
+  float* lse;
+  int B, H, N, d;
+  int nsplit;          // slices present
+  int keys_per_split;
+  int causal;
 };
 
 struct BwdParams {
@@ -65,6 +82,10 @@ cudaError_t launch_bwd_dot(const BwdParams& p, int elt, cudaStream_t s);
 // cudaErrorNotSupported for shapes it does not take.  Tensor maps are built
 // inside from the raw pointers.
 cudaError_t launch_fwd_tc16(const FwdParams& p, cudaStream_t s, bool causal);
+// split-KV partial pass of the tensor-core forward (writes p.o_part, p.lse_part)
+cudaError_t launch_fwd_tc16_partial(const FwdParams& p, cudaStream_t s, bool causal);
+// out_elt: 0 float32, 1 bf16, 2 fp16 storage of the merged O
+cudaError_t launch_merge(const MergeParams& p, int out_elt, cudaStream_t s);
 // phase 1: dQ kernel (also refines D in the workspace); phase 2: dK/dV kernel.
 cudaError_t launch_bwd_tc16(const BwdParams& p, cudaStream_t s, bool causal, int phase);
 

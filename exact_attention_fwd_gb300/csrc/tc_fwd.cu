@@ -131,21 +131,73 @@ struct Item {
   int tile[kQT];   // Q tile index, or -1
   int nblk[kQT];   // K blocks each tile visits
   int nmax;
+  int j0;          // first K block of the item (split-KV: the slice's first block)
+  int split;       // key slice (split-KV), else 0
 };
 
-template <bool kCausal>
-__device__ __forceinline__ Item decode_item(int it, int nq, int nk, int H) {
+// Split-KV work items of one head, in the causal case.  Pair p (tiles 2p and
+// 2p+1) has keys in blocks [0, 2p+2), i.e. ceil((p+1)/hb) slices of 2 hb
+// blocks, so the pairs fall into groups k = 1, 2, ... of hb pairs with k slices
+// each, and hb (k-1) k / 2 items come before group k.
+__host__ __device__ __forceinline__ long long causal_split_items(int npairs, int hb) {
+  const long long F = npairs / hb, r = npairs % hb;
+  return hb * F * (F + 1) / 2 + r * (F + 1);
+}
+__device__ __forceinline__ void causal_split_decode(int x, int hb, int& pr, int& sl) {
+  int k = static_cast<int>(0.5f * (1.0f + sqrtf(1.0f + 8.0f * static_cast<float>(x) /
+                                                        static_cast<float>(hb))));
+  k = max(k, 1);
+  while (k > 1 && static_cast<long long>(hb) * (k - 1) * k / 2 > x) --k;
+  while (static_cast<long long>(hb) * k * (k + 1) / 2 <= x) ++k;
+  const int off = x - static_cast<int>(static_cast<long long>(hb) * (k - 1) * k / 2);
+  pr = (k - 1) * hb + off / k;
+  sl = off % k;
+}
+
+// Work items of the whole launch.  Split-KV: one item per (tile pair, key
+// slice) that the pair's longer tile reads.
+__host__ __device__ __forceinline__ long long fwd_items(int B, int H, int nq, int nk, bool causal,
+                                                         bool split, int split_blocks) {
   const int npairs = (nq + 1) / 2;
-  const int bh = it / npairs, pr = it % npairs;
+  long long per_head = npairs;
+  if (split)
+    per_head = causal ? causal_split_items(npairs, split_blocks / 2)
+                      : static_cast<long long>(npairs) * ((nk + split_blocks - 1) / split_blocks);
+  return per_head * B * H;
+}
+
+template <bool kCausal, bool kSplit>
+__device__ __forceinline__ Item decode_item(int it, int nq, int nk, int H, int split_blocks) {
+  const int npairs = (nq + 1) / 2;
   Item r;
+  int bh, pr, sl = 0;
+  if constexpr (!kSplit) {
+    bh = it / npairs;
+    pr = it % npairs;
+  } else if constexpr (kCausal) {
+    const int per_head = static_cast<int>(causal_split_items(npairs, split_blocks / 2));
+    bh = it / per_head;
+    causal_split_decode(it % per_head, split_blocks / 2, pr, sl);
+  } else {
+    const int ns = (nk + split_blocks - 1) / split_blocks;
+    bh = it / (npairs * ns);
+    pr = (it / ns) % npairs;
+    sl = it % ns;
+  }
   r.b = bh / H;
   r.h = bh % H;
+  r.split = sl;
+  r.j0 = kSplit ? sl * split_blocks : 0;
   const int lo = 2 * pr, hi = 2 * pr + 1;
   r.tile[0] = (hi < nq) ? hi : lo;
   r.tile[1] = (hi < nq) ? lo : -1;
 #pragma unroll
-  for (int g = 0; g < kQT; ++g)
-    r.nblk[g] = (r.tile[g] < 0) ? 0 : (kCausal ? min(nk, r.tile[g] + 1) : nk);
+  for (int g = 0; g < kQT; ++g) {
+    const int all = (r.tile[g] < 0) ? 0 : (kCausal ? min(nk, r.tile[g] + 1) : nk);
+    // a slice's blocks [j0, j0 + split_blocks); a tile with none of them is idle
+    r.nblk[g] = kSplit ? max(0, min(all, r.j0 + split_blocks) - r.j0) : all;
+    if (r.nblk[g] == 0) r.tile[g] = -1;
+  }
   r.nmax = max(r.nblk[0], r.nblk[1]);
   return r;
 }
@@ -164,7 +216,7 @@ __device__ __forceinline__ int item_index(int li, int num_items) {
   return it < num_items ? static_cast<int>(it) : -1;
 }
 
-template <int DP, bool kCausal, bool kF16>
+template <int DP, bool kCausal, bool kF16, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -181,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = p.N, H = p.H;
   const int nq = (N + kBM - 1) / kBM;           // Q tiles per head
   const int nk = (N + kBN - 1) / kBN;           // K blocks per head
-  const int num_items = ((nq + 1) / 2) * p.B * H;
+  const int num_items =
+      static_cast<int>(fwd_items(p.B, H, nq, nk, kCausal, kSplit, p.split_blocks));
 
   // ---- setup: barriers, TMEM ----
   if (threadIdx.x == 0) {
@@ -245,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int li = 0;            // items started by this CTA
       bool ok = true;
       for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(li, num_items)) {
-        const Item w = decode_item<kCausal>(it, nq, nk, H);
+        const Item w = decode_item<kCausal, kSplit>(it, nq, nk, H, p.split_blocks);
         if constexpr (!Cfg::kSepP) {   // separate-P layout: Q comes from warp 3
           if (li > 0 && !mbar_wait(&bars->q_empty[0][0], (li - 1) & 1, abort_flag, kWaitBudget)) {
             ok = false;
@@ -269,11 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&bars->k_full[s], Cfg::kTileBytes);
           for (int ch = 0; ch < Cfg::kChunks; ++ch)
             tma_load_4d(sK + s * Cfg::kTileBytes + ch * kChunkBytes, &tmK, &bars->k_full[s],
-                        ch * 64, w.h, j * kBN, w.b);
+                        ch * 64, w.h, (w.j0 + j) * kBN, w.b);
           mbar_arrive_expect_tx(&bars->v_full[s], Cfg::kTileBytes);
           for (int ch = 0; ch < Cfg::kChunks; ++ch)
             tma_load_4d(sV + s * Cfg::kTileBytes + ch * kChunkBytes, &tmV, &bars->v_full[s],
-                        ch * 64, w.h, j * kBN, w.b);
+                        ch * 64, w.h, (w.j0 + j) * kBN, w.b);
           ++c;
         }
       }
@@ -295,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int qn[kQT] = {0, 0};   // Q loads per slot; load n uses buffer n & 1
       bool ok = true;
       for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
-        const Item w = decode_item<kCausal>(it, nq, nk, H);
+        const Item w = decode_item<kCausal, kSplit>(it, nq, nk, H, p.split_blocks);
         for (int g = 0; g < kQT; ++g) {
           if (w.tile[g] < 0) continue;
           const int b = qn[g] & 1, u = qn[g] >> 1;
@@ -374,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = warp - 1;
         int qn = 0;
         for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
-          const Item w = decode_item<kCausal>(it, nq, nk, H);
+          const Item w = decode_item<kCausal, kSplit>(it, nq, nk, H, p.split_blocks);
           const int nb = w.nblk[g];
           const int qb = qn & 1;   // Q buffer of this item (its load number is qn)
           if (nb > 0) {
@@ -417,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
-          const Item w = decode_item<kCausal>(it, nq, nk, H);
+          const Item w = decode_item<kCausal, kSplit>(it, nq, nk, H, p.split_blocks);
           if (!warp_wait(&bars->q_full[0][0], li & 1, abort_flag, kWaitBudget) ||
               !warp_wait(&bars->k_full[c % S], (c / S) & 1, abort_flag, kWaitBudget)) {
             ok = false;
@@ -509,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int li = 0;
     for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
-      const Item w = decode_item<kCausal>(it, nq, nk, H);
+      const Item w = decode_item<kCausal, kSplit>(it, nq, nk, H, p.split_blocks);
       const int qt = w.tile[g];
       if (qt < 0) {
         if constexpr (Cfg::kSepP) {
@@ -551,8 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ragged last block) set them to -inf before the row max: key k0 + i
         // is masked when i > lim (beyond N, or after q_row).  One copy of the
         // row loops serves every block (the instruction cache holds it once).
-        if ((kCausal && j == qt) || ((j + 1) * kBN > N)) {
-          const int k0 = j * kBN;
+        const int jb = w.j0 + j;   // the block's index among the head's keys
+        if ((kCausal && jb == qt) || ((jb + 1) * kBN > N)) {
+          const int k0 = jb * kBN;
           const int lim = min(N - k0 - 1, kCausal ? q_row - k0 : kBN);
 #pragma unroll
           for (int i = 0; i < kBN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
@@ -672,7 +726,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live = l > 0.0f;
       const float inv = live ? 1.0f / l : 0.0f;
       const bool store = q_row < N;
-      if constexpr (Cfg::kSepP) {
+      if constexpr (kSplit) {
+        // split-KV partial: O normalised over the slice, float32, straight
+        // from registers (one 16-byte store per 4 columns of the row)
+        float* orow = p.o_part +
+                      ((static_cast<size_t>(w.split) * p.B + w.b) * N + (store ? q_row : 0)) *
+                          static_cast<size_t>(H) * p.d +
+                      static_cast<size_t>(w.h) * p.d;
+#pragma unroll
+        for (int cc = 0; cc < DP / 32; ++cc) {
+          uint32_t orr[32];
+          __syncwarp();   // the stores below are per-thread; tcgen05.ld is collective
+          tmem_ld32(tO + cc * 32, orr);
+          tmem_ld_wait(orr);
+          if (store) {
+#pragma unroll
+            for (int qv = 0; qv < 8; ++qv) {
+              const int col = cc * 32 + qv * 4;
+              if (col < p.d)
+                *reinterpret_cast<float4*>(orow + col) =
+                    make_float4(__uint_as_float(orr[qv * 4 + 0]) * inv,
+                                __uint_as_float(orr[qv * 4 + 1]) * inv,
+                                __uint_as_float(orr[qv * 4 + 2]) * inv,
+                                __uint_as_float(orr[qv * 4 + 3]) * inv);
+            }
+          }
+        }
+      } else if constexpr (Cfg::kSepP) {
         // Stage the bf16 O tile in shared memory in the TMA box layout (rows
         // of 128 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7)), then
         // one thread stores it with a TMA tensor store (rows >= N and columns
@@ -756,9 +836,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      if (store)
-        p.lse[(static_cast<size_t>(w.b) * H + w.h) * N + q_row] =
-            live ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (store) {
+        const float L = live ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if constexpr (kSplit)
+          p.lse_part[((static_cast<size_t>(w.split) * p.B + w.b) * H + w.h) * N + q_row] = L;
+        else
+          p.lse[(static_cast<size_t>(w.b) * H + w.h) * N + q_row] = L;
+      }
     }
     if (!ok) raise_abort(bars, p.status);
     // the O stores must have completed (and read shared memory) before exit
@@ -790,20 +874,24 @@ int sm_count() {
   return n;
 }
 
-template <int DP, bool kCausal, bool kF16>
+template <int DP, bool kCausal, bool kF16, bool kSplit>
 cudaError_t launch_tc(const FwdParams& p, cudaStream_t st) {
   using Cfg = FwdCfg<DP>;
   CUtensorMap mq, mk, mv, mo;
   cudaError_t e = make_bhnd_tmap(&mq, p.q, p.B, p.N, p.H, p.d, kBM, 64, kF16);
   if (e == cudaSuccess) e = make_bhnd_tmap(&mk, p.k, p.B, p.N, p.H, p.d, kBM, 64, kF16);
   if (e == cudaSuccess) e = make_bhnd_tmap(&mv, p.v, p.B, p.N, p.H, p.d, kBM, 64, kF16);
-  if (e == cudaSuccess) e = make_bhnd_tmap(&mo, p.o, p.B, p.N, p.H, p.d, kBM, 64, kF16);
+  // the split-KV partial pass writes float32 rows directly; its O map is unused
+  if (e == cudaSuccess)
+    e = make_bhnd_tmap(&mo, kSplit ? p.q : p.o, p.B, p.N, p.H, p.d, kBM, 64, kF16);
   if (e != cudaSuccess) return e;
-  auto kern = fwd_tc_kernel<DP, kCausal, kF16>;
+  auto kern = fwd_tc_kernel<DP, kCausal, kF16, kSplit>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nq = (p.N + kBM - 1) / kBM;
-  const long long items = static_cast<long long>((nq + 1) / 2) * p.B * p.H;
+  const int nk = (p.N + kBN - 1) / kBN;
+  if (kSplit && (p.split_blocks < 2 || p.split_blocks % 2 != 0)) return cudaErrorInvalidValue;
+  const long long items = fwd_items(p.B, p.H, nq, nk, kCausal, kSplit, p.split_blocks);
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
@@ -814,18 +902,25 @@ cudaError_t launch_tc(const FwdParams& p, cudaStream_t st) {
                           Cfg::kSmemBytes, st);
 }
 
-template <bool kF16>
+template <bool kF16, bool kSplit>
 cudaError_t launch_dtype(const FwdParams& p, cudaStream_t s, bool causal) {
-  if (p.d <= 64) return causal ? launch_tc<64, true, kF16>(p, s) : launch_tc<64, false, kF16>(p, s);
+  if (p.d <= 64)
+    return causal ? launch_tc<64, true, kF16, kSplit>(p, s)
+                  : launch_tc<64, false, kF16, kSplit>(p, s);
   if (p.d <= 128)
-    return causal ? launch_tc<128, true, kF16>(p, s) : launch_tc<128, false, kF16>(p, s);
+    return causal ? launch_tc<128, true, kF16, kSplit>(p, s)
+                  : launch_tc<128, false, kF16, kSplit>(p, s);
   return cudaErrorNotSupported;
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_tc16(const FwdParams& p, cudaStream_t s, bool causal) {
-  return p.f16 ? launch_dtype<true>(p, s, causal) : launch_dtype<false>(p, s, causal);
+  return p.f16 ? launch_dtype<true, false>(p, s, causal) : launch_dtype<false, false>(p, s, causal);
+}
+
+cudaError_t launch_fwd_tc16_partial(const FwdParams& p, cudaStream_t s, bool causal) {
+  return p.f16 ? launch_dtype<true, true>(p, s, causal) : launch_dtype<false, true>(p, s, causal);
 }
 
 }  // namespace fa

@@ -164,6 +164,98 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          int B, int H, int N, int d, float scale, int causal,
                          fa_dtype dtype, fa_dtype grad_dtype, void* stream);
 
+/*
+ * Split-KV forward: the keys of each head are cut into slices, every
+ * (Q tile, key slice) pair is an independent piece of work, and the per-slice
+ * results are merged afterwards.  This spreads a few long heads over every SM
+ * (few heads x long N, where whole Q tiles are too few to fill the GPU), and
+ * the merge is the exchange step a context-parallel forward would need.
+ *
+ * Source: "Flash Attention 2 — forward pass notes", section "Loop (per
+ * (b, h, Q-tile))": the softmax of a concatenation of key blocks is the
+ * merge of the blocks' (m, l) states; and the "Lesson K23, fused attention"
+ * facts page, `sources.onlineSoftmax.claims[2]`: the (m, l) pairs combine
+ * with an associative, commutative operator, so the reduction may run in
+ * parallel and in any order.
+ *
+ * Slices: keys [s*keys_per_split, (s+1)*keys_per_split) for
+ * s < num_splits = ceil(N / keys_per_split).  Row i READS slice s when it
+ * sees at least one key there: with causal, iff s*keys_per_split <= i;
+ * without, always.
+ */
+
+/*
+ * fa_fwd_partial — attention of every query row over each key slice alone.
+ * For every (row i, slice s) that row i reads:
+ *   lse_part[s, b, h, i] = log sum_{j in s, visible} exp(scale q_i.k_j)
+ *   o_part[s, b, i, h, :] = sum_{j in s, visible} exp(scale q_i.k_j - lse_part) v_j
+ * (O normalised over the slice; float32, no rounding to 16 bits).  Entries of
+ * slices a row does not read are not written.
+ *
+ *   q, k, v        in : [B, N, H, d], element type `dtype` (BF16 or F16;
+ *                       F32 returns FA_ERR_UNSUPPORTED)
+ *   o_part        out : [num_splits, B, N, H, d] float32, 16-byte aligned
+ *   lse_part      out : [num_splits, B, H, N] float32
+ *   keys_per_split    : a positive multiple of 256
+ *   other arguments as in fa_fwd.  Outputs must not overlap inputs or each other.
+ */
+fa_status fa_fwd_partial(const void* q, const void* k, const void* v,
+                         float* o_part, float* lse_part,
+                         int B, int H, int N, int d, float scale, int causal,
+                         fa_dtype dtype, int keys_per_split, void* stream);
+
+/*
+ * fa_merge — combine per-slice results into the attention output.  For each
+ * row i, over the slices s it reads (see above) whose lse_part is not -inf:
+ *   L_i = log sum_s exp(lse_part[s, i]),
+ *   O_i = sum_s exp(lse_part[s, i] - L_i) o_part[s, i]
+ * (the (m, l) merge, with every slice's state written as m = lse, l = 1).
+ * A slice whose lse_part is -inf contributes nothing and its o_part is not
+ * read; a row with no contribution gets O = 0 and L = -inf.  O is rounded
+ * once to `dtype`.
+ *
+ *   o_part, lse_part  in : as written by fa_fwd_partial (any producer that
+ *                          follows the same layout and slice rule)
+ *   num_splits           : >= 1 slices present in o_part / lse_part; row i
+ *                          reads at most ceil(N / keys_per_split) of them
+ *   keys_per_split       : >= 1 (the slice width the partials were made with)
+ *   o                out : [B, N, H, d], element type `dtype` (F32, BF16, F16),
+ *                          16-byte aligned
+ *   lse              out : [B, H, N] float32
+ */
+fa_status fa_merge(const float* o_part, const float* lse_part, int num_splits,
+                   int keys_per_split, int causal, void* o, float* lse,
+                   int B, int H, int N, int d, fa_dtype dtype, void* stream);
+
+/*
+ * fa_fwd_splitkv_keys_per_split — the slice width fa_fwd_splitkv uses for
+ * `num_splits` requested slices: 256 * ceil(N / (256 num_splits)).  The
+ * slices actually used, ceil(N / that), may be fewer than requested.
+ * Returns 0 for non-positive arguments.
+ */
+int fa_fwd_splitkv_keys_per_split(int N, int num_splits);
+
+/*
+ * fa_fwd_splitkv_workspace_size — bytes of device workspace fa_fwd_splitkv
+ * needs for `num_splits` requested slices: o_part and lse_part for the
+ * slices used, each rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
+
+/*
+ * fa_fwd_splitkv — fa_fwd computed as fa_fwd_partial then fa_merge on one
+ * stream, with o_part and lse_part in `workspace` (o_part first, then
+ * lse_part at the next 256-byte boundary).  Same results as fa_fwd up to
+ * rounding order.  num_splits >= 1 (see fa_fwd_splitkv_keys_per_split);
+ * workspace 256-byte aligned, >= fa_fwd_splitkv_workspace_size(...) bytes,
+ * not overlapping any argument.  Other arguments as in fa_fwd; dtype BF16 or
+ * F16.
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, float scale, int causal,
+                         fa_dtype dtype, int num_splits,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
 /* fa_status_string — static, human-readable name of a status code. */
 const char* fa_status_string(fa_status s);
 

@@ -17,6 +17,8 @@ online_softmax   an independent restatement of the tiled online-softmax
 brute            scalar-loop attention for tiny inputs (no matrix routines).
 checker          tolerance comparison with mismatch counting.
 fp16_softmax     naive vs max-subtracted softmax rounded to fp16 (overflow pins).
+split_kv         attention over key slices and the (m, l, O) merge of the slice
+                 results (the split-KV forward).
 
 Parity status: every function here is pinned by tests/test_oracle_*.py against
 values printed on the pages (tests/golden/), closed forms, invariants, brute

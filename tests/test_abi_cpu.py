@@ -97,3 +97,66 @@ def test_bwd_phase_rejects_bad_phase(lib):
     assert _lib.fa_bwd_phase(-1, **a) == 1
     a["workspace"] = 0
     assert _lib.fa_bwd_phase(1, **a) == 1
+
+
+def test_splitkv_sizes(lib):
+    from exact_attention_fwd_gb300 import _lib
+    assert _lib.fa_fwd_splitkv_keys_per_split(8192, 4) == 2048
+    assert _lib.fa_fwd_splitkv_keys_per_split(1000, 3) == 512      # 2 slices used
+    assert _lib.fa_fwd_splitkv_keys_per_split(100, 8) == 256
+    assert _lib.fa_fwd_splitkv_keys_per_split(0, 2) == 0
+    assert _lib.fa_fwd_splitkv_keys_per_split(10, 0) == 0
+    # 2 slices of [1, 1000, 2, 64] float32 + 2 slices of [1, 2, 1000] float32
+    assert _lib.fa_fwd_splitkv_workspace_size(1, 2, 1000, 64, 3) == 1024000 + 16128
+    assert _lib.fa_fwd_splitkv_workspace_size(1, 2, 1000, 64, 0) == 0
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(o_part=0), 1),
+    (dict(keys_per_split=128), 1),         # not a multiple of 256
+    (dict(keys_per_split=0), 1),
+    (dict(dtype=0), 2),                    # float32 inputs: not on this path
+    (dict(d=136), 2),
+    (dict(o_part=FAKE + 8), 1),            # misaligned
+    (dict(o_part=FAKE), 1),                # overlaps q
+    (dict(lse_part=4 * FAKE + 64), 1),     # overlaps o_part
+])
+def test_fwd_partial_rejects_invalid_arguments(lib, kw, want):
+    from exact_attention_fwd_gb300 import _lib
+    a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o_part=4 * FAKE, lse_part=8 * FAKE, B=1, H=1, N=16,
+             d=64, scale=0.125, causal=1, dtype=1, keys_per_split=256, stream=None)
+    a.update(kw)
+    assert _lib.fa_fwd_partial(**a) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(lse=0), 1),
+    (dict(num_splits=0), 1), (dict(keys_per_split=0), 1),
+    (dict(dtype=5), 1),
+    (dict(o=FAKE + 4), 1),                 # misaligned
+    (dict(o=FAKE + 64), 1),                # overlaps o_part
+    (dict(N=0), 1),
+])
+def test_merge_rejects_invalid_arguments(lib, kw, want):
+    from exact_attention_fwd_gb300 import _lib
+    a = dict(o_part=FAKE, lse_part=2 * FAKE, num_splits=2, keys_per_split=256, causal=1,
+             o=4 * FAKE, lse=5 * FAKE, B=1, H=1, N=16, d=64, dtype=1, stream=None)
+    a.update(kw)
+    assert _lib.fa_merge(**a) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(workspace=0), 1),
+    (dict(num_splits=0), 1),
+    (dict(workspace_bytes=64), 1),
+    (dict(workspace=8 * FAKE + 16), 1),    # not 256-byte aligned
+    (dict(workspace=FAKE), 1),             # overlaps q
+    (dict(dtype=0), 2),
+])
+def test_splitkv_rejects_invalid_arguments(lib, kw, want):
+    from exact_attention_fwd_gb300 import _lib
+    a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, B=1, H=1, N=16, d=64,
+             scale=0.125, causal=1, dtype=1, num_splits=2, workspace=8 * FAKE,
+             workspace_bytes=1 << 20, stream=None)
+    a.update(kw)
+    assert _lib.fa_fwd_splitkv(**a) == want
