@@ -7,28 +7,35 @@
 // global memory; the per-row log-sum-exp L = m + log l is written at the end.
 //
 // GB300 mapping: a persistent kernel, one CTA per SM, 12 warps.
-//   * Work item = two 128-row Q tiles of one (b, h).  With the causal mask the
-//     pair is (i, nq-1-i): tile i sees i+1 key blocks and tile nq-1-i sees
-//     nq-i, so every item has the same nq+1 block-tiles of work and a static
-//     round-robin schedule is balanced.  Items are numbered head-major, so the
-//     CTAs working at one time share a few heads' K/V through L2.  Both tiles
-//     share every K/V block they both need.
-//   * warp 0 (one lane) issues TMA tile loads: the item's Q tiles, then K_j
-//     and V_j into a ring of shared-memory stages guarded by full/empty
+//   * Work item = two adjacent 128-row Q tiles (2p, 2p+1) of one (b, h); both
+//     read every K/V block the shorter one needs, so each block is loaded once
+//     for the pair.  Items are numbered head-major, so the CTAs working at one
+//     time share a few heads' K/V through L2; the static round-robin schedule
+//     runs odd waves in reverse CTA order, pairing a CTA's short causal items
+//     with long ones.
+//   * Split-KV mode (kSplit): an item is (tile pair, key slice); the tiles
+//     visit only the slice's blocks and write O normalised over the slice and
+//     the slice's L, in float32, for a separate merge kernel.
+//   * warp 0 (one lane) issues TMA tile loads: K_j and V_j (and with d = 128
+//     the item's Q tiles) into a ring of shared-memory stages guarded by full/empty
 //     mbarriers.  The ring's position and every barrier's phase carry over
 //     from item to item, so the next item's loads overlap this item's tail.
-//   * warp 1 (one lane) issues tcgen05 MMAs: S_g = Q_g K_j^T (both operands
+//   * one lane issues the tcgen05 MMAs: S_g = Q_g K_j^T (both operands
 //     K-major in smem, fp32 accumulator in TMEM) and O_g += P_g V_j (P read
-//     from TMEM, V as an MN-major smem operand).  The two tiles' MMAs
-//     interleave, so one tile's softmax overlaps the other tile's MMAs.
+//     from TMEM, V as an MN-major smem operand).  With d <= 64 warps 1 and 2
+//     each issue one tile's MMAs and warp 3 loads Q (two buffers per tile, so
+//     the next item's Q lands early); with d = 128 warp 1 interleaves both
+//     tiles' MMAs.  Either way one tile's softmax overlaps the other tile's
+//     MMAs.
 //   * warps 4-7 and 8-11 are the softmax warpgroups of tiles 0 and 1: one
 //     thread per query row (= TMEM lane) loads its row of S, masks, takes the
 //     row max, exponentiates in base 2 with scale*log2(e) folded in, writes P
-//     as bf16 back into the same TMEM columns, and keeps m and l in registers.
+//     as 16-bit pairs into TMEM (its own columns with d <= 64, over S's with
+//     d = 128), and keeps m and l in registers.
 //     O is rescaled by alpha = 2^(m_old - m_new) in TMEM only when the running
 //     max rises by more than kRescaleThreshold (log2 units); a stale reference
 //     max cancels exactly in O / l and in L.  After an item's last block each
-//     thread divides its O row by l, rounds once to bf16 and stores it, and
+//     thread divides its O row by l, rounds once to 16 bits and stores it, and
 //     stores L in natural-log units; meanwhile the MMA warp already computes
 //     the next item's first scores.
 //   * the producer/MMA warpgroup gives registers to the softmax warpgroups
