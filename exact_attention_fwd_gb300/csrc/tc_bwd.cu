@@ -72,7 +72,7 @@ namespace {
 
 constexpr int kRows = 128;       // rows owned by a work item
 constexpr int kThreads = 384;
-constexpr int kRegsHelper = 80;    // warps 0-3: TMA, MMA, vectors, fp16 copy
+constexpr int kRegsHelper = 88;    // warps 0-3: TMA, MMA, vectors, fp16 copy
 constexpr int kRegsElem = 208;     // warps 4-11: element-wise and epilogue
 static_assert(4 * 32 * kRegsHelper + 8 * 32 * kRegsElem <= 168 * kThreads,
               "register split exceeds the launch allocation");

@@ -70,7 +70,7 @@ constexpr int kThreads = 384;            // 12 warps
 constexpr int kChunkBytes = kBM * 128;   // one 64-column swizzled chunk of 128 rows
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kRegsLoad = 64;            // warps 0-3 (TMA, MMA, idle)
+constexpr int kRegsLoad = 72;            // warps 0-3 (TMA, MMA, Q loads)
 constexpr int kRegsSoftmax = 216;        // warps 4-11
 static_assert(4 * 32 * kRegsLoad + 8 * 32 * kRegsSoftmax <= 168 * kThreads,
               "register split exceeds the launch allocation");
