@@ -329,13 +329,15 @@ def run_ours(args, rank, local_rank, world):
         Ke = max(3, min(K, args.e2e_steps))
         out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                     for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        outs = tuple(out_host[n] for n in ("o", "lse", "dq", "dk", "dv"))
+        chunk = min(args.e2e_chunk, B)
+        hws = api.host_workspace(chunk, H, N, d, torch.bfloat16, torch.bfloat16, dev)
 
         def e2e_step():
-            qd, kd, vd, dod = (host[t].to(dev, non_blocking=True) for t in ("q", "k", "v", "do"))
-            oo, ll = api.forward(qd, kd, vd, scale=scale, causal=causal)
-            gq, gk, gv = api.backward(qd, kd, vd, oo, ll, dod, scale=scale, causal=causal, ws=ws)
-            for n, t in (("o", oo), ("lse", ll), ("dq", gq), ("dk", gk), ("dv", gv)):
-                out_host[n].copy_(t, non_blocking=True)
+            # host buffers in, host buffers out: fa_fwd_bwd_host overlaps the
+            # copies of one batch chunk with the kernels of the next
+            api.fwd_bwd_host(host["q"], host["k"], host["v"], host["do"], chunk, scale=scale,
+                             causal=causal, out=outs, ws=hws, device=dev)
 
         e2e_step()
         torch.cuda.synchronize(dev)
@@ -352,7 +354,8 @@ def run_ours(args, rank, local_rank, world):
         d2h = sum(t.numel() * t.element_size() for t in out_host.values())
         e2e = {"value": round(world * Ke * (fwd_fl + bwd_fl) / (te / 1e3) / 1e12, 2),
                "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(te / Ke, 3), "steps": Ke}
+               "ms_per_step": round(te / Ke, 3), "steps": Ke, "api": "fa_fwd_bwd_host",
+               "batch_chunk": chunk}
         if api.sync_status() != 0:
             raise SystemExit("device status word set during the end-to-end run")
 
@@ -442,6 +445,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-chunk", type=int, default=8,
+                    help="sequences per copy/compute chunk of the end-to-end call")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

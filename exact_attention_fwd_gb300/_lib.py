@@ -16,7 +16,8 @@ FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F16 = range(3)
 
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_phase", "fa_bwd_workspace_size", "fa_sync_status",
            "fa_status_string", "fa_bwd_noalloc", "fa_fwd_partial", "fa_merge",
-           "fa_fwd_splitkv_keys_per_split", "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv")
+           "fa_fwd_splitkv_keys_per_split", "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv",
+           "fa_fwd_bwd_host_workspace_size", "fa_fwd_bwd_host")
 FA_BWD_NOALLOC_MAX_ROWS = 1 << 22
 
 _lib = None
@@ -60,6 +61,11 @@ def load():
     lib.fa_fwd_splitkv_workspace_size.restype = sz
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp, sz, vp]
     lib.fa_fwd_splitkv.restype = i
+    lib.fa_fwd_bwd_host_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.fa_fwd_bwd_host_workspace_size.restype = sz
+    lib.fa_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, i,
+                                    vp, sz, vp]
+    lib.fa_fwd_bwd_host.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -128,3 +134,16 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, num_splits
                    workspace_bytes, stream):
     return load().fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, float(scale), int(causal),
                                  int(dtype), int(num_splits), workspace, workspace_bytes, stream)
+
+
+def fa_fwd_bwd_host_workspace_size(batch_chunk, H, N, d, dtype, grad_dtype):
+    return int(load().fa_fwd_bwd_host_workspace_size(batch_chunk, H, N, d, int(dtype),
+                                                     int(grad_dtype)))
+
+
+def fa_fwd_bwd_host(q, k, v, dO, o, lse, dq, dk, dv, B, H, N, d, scale, causal, dtype, grad_dtype,
+                    batch_chunk, workspace, workspace_bytes, stream):
+    """Host pointers for the tensors, a device workspace; see include/fa.h."""
+    return load().fa_fwd_bwd_host(q, k, v, dO, o, lse, dq, dk, dv, B, H, N, d, float(scale),
+                                  int(causal), int(dtype), int(grad_dtype), int(batch_chunk),
+                                  workspace, workspace_bytes, stream)

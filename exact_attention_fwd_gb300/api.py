@@ -175,6 +175,60 @@ def forward_splitkv(q, k, v, num_splits, scale=None, causal=False, out=None, lse
     return out, lse
 
 
+def _check_host(t, name, dtype):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def host_workspace(batch_chunk, H, N, d, dtype, grad_dtype, device):
+    """A device workspace tensor sized for fwd_bwd_host."""
+    n = _lib.fa_fwd_bwd_host_workspace_size(batch_chunk, H, N, d, _DTYPES[dtype], _DTYPES[grad_dtype])
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def fwd_bwd_host(q, k, v, do, batch_chunk, scale=None, causal=False, grad_dtype=None, out=None,
+                 ws=None, device=None, stream=None):
+    """Forward and backward on host tensors (fa_fwd_bwd_host): copies in, both
+    passes and copies out, pipelined over chunks of `batch_chunk` sequences.
+
+    q, k, v, do: [B, N, H, d] CPU tensors (pinned for overlap).  Returns the
+    host tensors (o, lse, dq, dk, dv), complete once `stream` is synchronised.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+        _check_host(t, name, q.dtype)
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, N, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    gdt = q.dtype if grad_dtype is None else grad_dtype
+    device = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    bc = min(batch_chunk, B)
+    if ws is None:
+        ws = host_workspace(bc, H, N, d, q.dtype, gdt, device)
+    if out is None:
+        pin = q.is_pinned()
+        out = (torch.empty(q.shape, dtype=q.dtype, pin_memory=pin),
+               torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin),
+               *(torch.empty(q.shape, dtype=gdt, pin_memory=pin) for _ in range(3)))
+    o, lse, dq, dk, dv = out
+    _check_host(o, "o", q.dtype)
+    _check_host(lse, "lse", torch.float32)
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_host(t, name, gdt)
+    st = _lib.fa_fwd_bwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                              o.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), B, H, N, d, scale, causal, _DTYPES[q.dtype],
+                              _DTYPES[gdt], batch_chunk, ws.data_ptr(), ws.numel(),
+                              _stream_handle(stream))
+    if st != _lib.FA_OK:
+        raise _lib.FaError(st, "fa_fwd_bwd_host")
+    return o, lse, dq, dk, dv
+
+
 def sync_status(stream=None):
     """Synchronise and return (and clear) the device status word."""
     return _lib.fa_sync_status(_stream_handle(stream))

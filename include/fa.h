@@ -256,6 +256,40 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
                          fa_dtype dtype, int num_splits,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * fa_fwd_bwd_host — fa_fwd then fa_bwd on HOST buffers: the inputs are copied
+ * in, the outputs copied out, all inside the call's stream order.  The pages
+ * have no counterpart; this is the library's end-to-end entry point.
+ *
+ * The batch is processed in chunks of `batch_chunk` sequences through two
+ * device slots in `workspace`, so that the copy-in of chunk c+1 and the
+ * copy-out of chunk c-1 overlap the kernels of chunk c (two internal copy
+ * streams, created once per device, plus the caller's stream for the
+ * kernels).  Host buffers should be page-locked (cudaHostAlloc /
+ * cudaHostRegister); pageable buffers give correct results without overlap.
+ *
+ *   q, k, v, dO      in : HOST, [B, N, H, d], element type `dtype`
+ *   o               out : HOST, [B, N, H, d], `dtype`
+ *   lse             out : HOST, [B, H, N] float32
+ *   dq, dk, dv      out : HOST, [B, N, H, d], `grad_dtype`
+ *   batch_chunk         : >= 1 sequences per chunk (min(batch_chunk, B) used)
+ *   workspace           : DEVICE, 256-byte aligned, >=
+ *                         fa_fwd_bwd_host_workspace_size(min(batch_chunk, B),
+ *                         H, N, d, dtype, grad_dtype) bytes
+ *   other arguments as in fa_fwd and fa_bwd.
+ * The call returns once everything is queued; the host outputs are complete
+ * after `stream` is synchronised (then also check fa_sync_status).  Host
+ * outputs must not overlap host inputs.  Concurrent calls on one device are
+ * queued one after another.
+ */
+size_t fa_fwd_bwd_host_workspace_size(int batch_chunk, int H, int N, int d, fa_dtype dtype,
+                                      fa_dtype grad_dtype);
+fa_status fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO,
+                          void* o, float* lse, void* dq, void* dk, void* dv,
+                          int B, int H, int N, int d, float scale, int causal,
+                          fa_dtype dtype, fa_dtype grad_dtype, int batch_chunk,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* fa_status_string — static, human-readable name of a status code. */
 const char* fa_status_string(fa_status s);
 

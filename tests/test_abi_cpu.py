@@ -160,3 +160,35 @@ def test_splitkv_rejects_invalid_arguments(lib, kw, want):
              workspace_bytes=1 << 20, stream=None)
     a.update(kw)
     assert _lib.fa_fwd_splitkv(**a) == want
+
+
+def test_host_workspace_size(lib):
+    from exact_attention_fwd_gb300 import _lib
+    # per slot: 5 bf16 tensors + 3 bf16 gradients of 2x16x2x64, L and D of 2x2x16 floats
+    t = 2 * 16 * 2 * 64 * 2
+    slot = 8 * t + 256 + 256
+    assert _lib.fa_fwd_bwd_host_workspace_size(2, 2, 16, 64, 1, 1) == 2 * slot
+    # float32 gradients of bf16 inputs
+    slot32 = 5 * t + 3 * 2 * t + 256 + 256
+    assert _lib.fa_fwd_bwd_host_workspace_size(2, 2, 16, 64, 1, 0) == 2 * slot32
+    assert _lib.fa_fwd_bwd_host_workspace_size(0, 2, 16, 64, 1, 1) == 0
+    assert _lib.fa_fwd_bwd_host_workspace_size(2, 2, 16, 64, 1, 2) == 0   # fp16 grads of bf16
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), 1), (dict(dv=0), 1), (dict(workspace=0), 1),
+    (dict(batch_chunk=0), 1),
+    (dict(workspace_bytes=1024), 1),
+    (dict(workspace=FAKE + 64), 1),        # not 256-byte aligned
+    (dict(d=12), 1), (dict(d=136), 2),
+    (dict(scale=float("nan")), 1),
+    (dict(grad_dtype=2), 1),
+])
+def test_host_rejects_invalid_arguments(lib, kw, want):
+    from exact_attention_fwd_gb300 import _lib
+    a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, dO=4 * FAKE, o=5 * FAKE, lse=6 * FAKE, dq=7 * FAKE,
+             dk=8 * FAKE, dv=9 * FAKE, B=4, H=2, N=16, d=64, scale=0.125, causal=1, dtype=1,
+             grad_dtype=1, batch_chunk=2, workspace=16 * FAKE, workspace_bytes=1 << 24,
+             stream=None)
+    a.update(kw)
+    assert _lib.fa_fwd_bwd_host(**a) == want
