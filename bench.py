@@ -359,6 +359,37 @@ def run_ours(args, rank, local_rank, world):
         if api.sync_status() != 0:
             raise SystemExit("device status word set during the end-to-end run")
 
+    # the unfused forward (S and P through global memory), timed alone on the
+    # same inputs, beside the fused forward's per-kernel time above
+    unfused = None
+    if not args.no_unfused:
+        uws = api.unfused_workspace(B, H, N, d, dev)
+        o_u, l_u = torch.empty_like(o), torch.empty_like(lse)
+
+        def unfused_fwd():
+            api.forward_unfused(q, k, v, scale=scale, causal=causal, out=o_u, lse=l_u, ws=uws)
+
+        for _ in range(3):
+            unfused_fwd()
+        torch.cuda.synchronize(dev)
+        Ku = 10
+        s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s3.record(stream)
+        for _ in range(Ku):
+            unfused_fwd()
+        e3.record(stream)
+        torch.cuda.synchronize(dev)
+        if api.sync_status() != 0:
+            raise SystemExit("device status word set during the unfused run")
+        tu = s3.elapsed_time(e3) / Ku
+        unfused = {"ms": round(tu, 4), "tflops": round(fwd_fl / (tu / 1e3) / 1e12, 1),
+                   "fused_fwd_ms": round(per["fwd_tc_kernel"], 4),
+                   "slowdown_vs_fused": round(tu / per["fwd_tc_kernel"], 2),
+                   # S written and read, P written and read (per head 4+4+2+2 N^2 bytes)
+                   "nxn_bytes_per_launch": 12 * B * H * N * N,
+                   "max_abs_diff_vs_fused": float((o_u.float() - o.float()).abs().max())}
+        del uws
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, nh, secs = cpu_oracle_rate(inp, scale, causal, args.cpu_seconds)
@@ -394,6 +425,7 @@ def run_ours(args, rank, local_rank, world):
                      "traffic": traffic_for(dom), "peak_source": peak_src + " (burst)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "unfused_fwd": unfused,
         "gpu_launches": 4 * K,
         "clocks": clk.summary(),
     }
@@ -449,6 +481,8 @@ def main(argv=None):
                     help="sequences per copy/compute chunk of the end-to-end call")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true",
+                    help="skip timing the unfused comparison forward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override B (profiler captures of a smaller case); 0 = the workload's")

@@ -17,7 +17,8 @@ FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F16 = range(3)
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_phase", "fa_bwd_workspace_size", "fa_sync_status",
            "fa_status_string", "fa_bwd_noalloc", "fa_fwd_partial", "fa_merge",
            "fa_fwd_splitkv_keys_per_split", "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv",
-           "fa_fwd_bwd_host_workspace_size", "fa_fwd_bwd_host")
+           "fa_fwd_bwd_host_workspace_size", "fa_fwd_bwd_host", "fa_fwd_unfused_workspace_size",
+           "fa_fwd_unfused")
 FA_BWD_NOALLOC_MAX_ROWS = 1 << 22
 
 _lib = None
@@ -66,6 +67,10 @@ def load():
     lib.fa_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, i,
                                     vp, sz, vp]
     lib.fa_fwd_bwd_host.restype = i
+    lib.fa_fwd_unfused_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_fwd_unfused_workspace_size.restype = sz
+    lib.fa_fwd_unfused.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+    lib.fa_fwd_unfused.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -147,3 +152,14 @@ def fa_fwd_bwd_host(q, k, v, dO, o, lse, dq, dk, dv, B, H, N, d, scale, causal, 
     return load().fa_fwd_bwd_host(q, k, v, dO, o, lse, dq, dk, dv, B, H, N, d, float(scale),
                                   int(causal), int(dtype), int(grad_dtype), int(batch_chunk),
                                   workspace, workspace_bytes, stream)
+
+
+def fa_fwd_unfused_workspace_size(B, H, N, d):
+    return int(load().fa_fwd_unfused_workspace_size(B, H, N, d))
+
+
+def fa_fwd_unfused(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, workspace, workspace_bytes,
+                   stream):
+    """The unfused comparison forward (include/fa.h)."""
+    return load().fa_fwd_unfused(q, k, v, o, lse, B, H, N, d, float(scale), int(causal),
+                                 int(dtype), workspace, workspace_bytes, stream)

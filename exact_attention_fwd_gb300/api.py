@@ -229,6 +229,34 @@ def fwd_bwd_host(q, k, v, do, batch_chunk, scale=None, causal=False, grad_dtype=
     return o, lse, dq, dk, dv
 
 
+def unfused_workspace(B, H, N, d, device):
+    """A device workspace tensor sized for forward_unfused (holds S, B H N^2 floats)."""
+    n = _lib.fa_fwd_unfused_workspace_size(B, H, N, d)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def forward_unfused(q, k, v, scale=None, causal=False, out=None, lse=None, ws=None, stream=None):
+    """The unfused forward (fa_fwd_unfused): S to global memory, a row softmax,
+    then P V; a comparison for forward()."""
+    _check_qkv(q, k, v)
+    B, N, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = unfused_workspace(B, H, N, d, q.device)
+    _check(out, "out", q.dtype)
+    _check(lse, "lse", torch.float32)
+    st = _lib.fa_fwd_unfused(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr(), B, H, N, d, scale, causal, _DTYPES[q.dtype],
+                             ws.data_ptr(), ws.numel(), _stream_handle(stream))
+    if st != _lib.FA_OK:
+        raise _lib.FaError(st, "fa_fwd_unfused")
+    return out, lse
+
+
 def sync_status(stream=None):
     """Synchronise and return (and clear) the device status word."""
     return _lib.fa_sync_status(_stream_handle(stream))

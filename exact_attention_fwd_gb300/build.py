@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfa.so")
 
 SOURCES = ("fa_api.cu", "simt_f32.cu", "bwd_dot.cu", "tc_fwd.cu", "tc_bwd.cu", "fa_noalloc.cu",
-           "merge.cu", "fa_host.cu")
+           "merge.cu", "fa_host.cu", "unfused.cu")
 ARCH = ("-gencode", "arch=compute_103a,code=sm_103a")
 NVCC_FLAGS = ("-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include"))
@@ -73,7 +73,8 @@ def build(force=False, verbose=False, ptxas_info=False):
             if log.strip():
                 print(f"--- {src}\n{log}", file=sys.stderr)
     tmp = LIB + ".tmp"
-    cmd = [exe, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-cudart", "static"]
+    cmd = [exe, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-cudart", "static",
+           "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

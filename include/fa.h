@@ -290,6 +290,36 @@ fa_status fa_fwd_bwd_host(const void* q, const void* k, const void* v, const voi
                           fa_dtype dtype, fa_dtype grad_dtype, int batch_chunk,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * fa_fwd_unfused — the unfused forward, kept as a measured comparison for
+ * fa_fwd (not the fused method).
+ *
+ * Source: "Lesson K23, fused attention" facts page, `sources.flashAttention`
+ * (Algorithm 0) and block `traffic`: S = scale Q K^T is written to global
+ * memory, a row softmax reads S and writes P, then O = P V reads P, so each
+ * head moves its N x N matrices through DRAM (4 N^2 bytes of extra memory).
+ * Here S is float32 [B, H, N, N] in `workspace`; the row softmax writes
+ * exp(S - m) (16-bit) over the first half of each S row and the row sums l;
+ * O = (exp(S - m) V) / l, the product in float32, divided and rounded once
+ * by the library's kernel.  The two matrix products are plain cuBLAS GEMMs
+ * (16-bit inputs, float32 accumulation) loaded on first use.  Same outputs
+ * as fa_fwd (o, lse), up to rounding.
+ *
+ *   q, k, v, o, lse, B, H, N, d, scale, causal : as in fa_fwd
+ *   dtype      : BF16 or F16 (F32 returns FA_ERR_UNSUPPORTED)
+ *   workspace  : DEVICE, 256-byte aligned, >= fa_fwd_unfused_workspace_size
+ *                (B, H, N, d) bytes: S (4 B H N^2), the float32 product
+ *                (4 B N H d), l (4 B H N), each rounded up to 256 bytes, then
+ *                the GEMMs' workspace (32 MiB)
+ * Returns FA_ERR_UNSUPPORTED if cuBLAS cannot be loaded.  The first call on
+ * a device creates a cuBLAS handle; calls are serialised on the host.
+ */
+size_t fa_fwd_unfused_workspace_size(int B, int H, int N, int d);
+fa_status fa_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, float scale, int causal,
+                         fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
 /* fa_status_string — static, human-readable name of a status code. */
 const char* fa_status_string(fa_status s);
 

@@ -192,3 +192,30 @@ def test_host_rejects_invalid_arguments(lib, kw, want):
              stream=None)
     a.update(kw)
     assert _lib.fa_fwd_bwd_host(**a) == want
+
+
+def test_unfused_workspace_size(lib):
+    from exact_attention_fwd_gb300 import _lib
+    # S (2 x 3 x 100 x 100 floats), O' (2 x 100 x 3 x 64 floats), l (2 x 3 x 100
+    # floats), each rounded up to 256 bytes, then 32 MiB for the GEMMs
+    assert _lib.fa_fwd_unfused_workspace_size(2, 3, 100, 64) == \
+        240128 + 153600 + 2560 + (32 << 20)
+    assert _lib.fa_fwd_unfused_workspace_size(0, 3, 100, 64) == 0
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), 1), (dict(workspace=0), 1),
+    (dict(workspace_bytes=1000), 1),
+    (dict(workspace=16 * FAKE + 128), 1),   # not 256-byte aligned
+    (dict(d=20), 1), (dict(d=136), 2),
+    (dict(dtype=0), 2),                     # float32: not on this path
+    (dict(q=FAKE + 4), 1),                  # misaligned
+    (dict(scale=float("inf")), 1),
+])
+def test_unfused_rejects_invalid_arguments(lib, kw, want):
+    from exact_attention_fwd_gb300 import _lib
+    a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, B=1, H=1, N=16, d=64,
+             scale=0.125, causal=1, dtype=1, workspace=16 * FAKE, workspace_bytes=1 << 26,
+             stream=None)
+    a.update(kw)
+    assert _lib.fa_fwd_unfused(**a) == want
