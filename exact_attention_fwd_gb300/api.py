@@ -257,6 +257,30 @@ def forward_unfused(q, k, v, scale=None, causal=False, out=None, lse=None, ws=No
     return out, lse
 
 
+def forward_tf32x3(q, k, v, scale=None, causal=False, out=None, lse=None, ws=None, stream=None):
+    """float32 O, LSE = attention(q, k, v) on the tensor cores (fa_fwd_tf32x3, d <= 64)."""
+    _check_qkv(q, k, v)
+    if q.dtype != torch.float32:
+        raise ValueError("forward_tf32x3 takes float32 tensors")
+    B, N, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = torch.empty(_lib.fa_fwd_tf32x3_workspace_size(B, H, N, d), dtype=torch.uint8,
+                         device=q.device)
+    _check(out, "out", torch.float32)
+    _check(lse, "lse", torch.float32)
+    st = _lib.fa_fwd_tf32x3(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr(), B, H, N, d, scale, causal, ws.data_ptr(), ws.numel(),
+                            _stream_handle(stream))
+    if st != _lib.FA_OK:
+        raise _lib.FaError(st, "fa_fwd_tf32x3")
+    return out, lse
+
+
 def sync_status(stream=None):
     """Synchronise and return (and clear) the device status word."""
     return _lib.fa_sync_status(_stream_handle(stream))

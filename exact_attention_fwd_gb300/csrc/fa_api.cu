@@ -393,3 +393,54 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// float32 forward on the tensor cores (3xTF32)
+// ---------------------------------------------------------------------------
+
+extern "C" {
+
+size_t fa_fwd_tf32x3_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  return fa::tf32x3_workspace_bytes(B, H, N, d);
+}
+
+fa_status fa_fwd_tf32x3(const float* q, const float* k, const float* v, float* o, float* lse,
+                        int B, int H, int N, int d, float scale, int causal, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (d > 64) return FA_ERR_UNSUPPORTED;
+  if (workspace_bytes < fa_fwd_tf32x3_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return FA_ERR_INVALID_ARG;
+  const size_t tbytes = static_cast<size_t>(B) * N * H * d * 4;
+  const size_t lbytes = static_cast<size_t>(B) * H * N * sizeof(float);
+  for (const void* in : {static_cast<const void*>(q), static_cast<const void*>(k),
+                         static_cast<const void*>(v)}) {
+    if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes) ||
+        overlaps(workspace, workspace_bytes, in, tbytes))
+      return FA_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, tbytes, lse, lbytes) || overlaps(workspace, workspace_bytes, o, tbytes) ||
+      overlaps(workspace, workspace_bytes, lse, lbytes))
+    return FA_ERR_INVALID_ARG;
+  fa_status err = FA_OK;
+  int* status = status_word(&err);
+  if (status == nullptr) return err;
+  fa::FwdParams p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+  p.B = B; p.H = H; p.N = N; p.d = d;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status;
+  p.probe_timeout = probe_timeout_requested() ? 1 : 0;
+  cudaError_t e = fa::launch_fwd_tf32x3(p, workspace, static_cast<cudaStream_t>(stream),
+                                        causal != 0);
+  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

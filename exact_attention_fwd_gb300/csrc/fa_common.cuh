@@ -86,6 +86,10 @@ cudaError_t launch_fwd_tc16(const FwdParams& p, cudaStream_t s, bool causal);
 cudaError_t launch_fwd_tc16_partial(const FwdParams& p, cudaStream_t s, bool causal);
 // out_elt: 0 float32, 1 bf16, 2 fp16 storage of the merged O
 cudaError_t launch_merge(const MergeParams& p, int out_elt, cudaStream_t s);
+// float32 forward on the tensor cores (3xTF32), d <= 64; workspace of
+// tf32x3_workspace_bytes() holds the hi/lo split of q, k, v
+size_t tf32x3_workspace_bytes(int B, int H, int N, int d);
+cudaError_t launch_fwd_tf32x3(const FwdParams& p, void* workspace, cudaStream_t s, bool causal);
 // phase 1: dQ kernel (also refines D in the workspace); phase 2: dK/dV kernel.
 cudaError_t launch_bwd_tc16(const BwdParams& p, cudaStream_t s, bool causal, int phase);
 

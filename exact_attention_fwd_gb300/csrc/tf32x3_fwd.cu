@@ -1,0 +1,523 @@
+// tf32x3_fwd.cu — float32 attention forward on the tensor cores (3xTF32).
+//
+// Algorithm: "Flash Attention 2 — forward pass notes", sections "Loop (per
+// (b, h, Q-tile))" and "What's still needed for full FA2" item 1, as in the
+// 16-bit kernel; here every input and output is float32.
+//
+// tcgen05 kind::tf32 multiplies 32-bit operands with 10 explicit mantissa
+// bits.  Each float32 x is split into hi = x rounded to the nearest tf32
+// value and lo = (x - hi) rounded to the nearest tf32 value (x - hi is exact
+// in float32 and |x - hi| <= 2^-11 |x|), and a product is taken as
+// hi*hi + hi*lo + lo*hi.  The dropped lo*lo term and the two roundings of lo
+// leave at most about 3 * 2^-22 relative error per product, and the operands
+// are already tf32 values, so how the tensor cores reduce 32-bit operands to
+// tf32 does not matter.
+//
+//   1. split pass (HBM-bound): Qh, Ql, Kh, Kl as [B, N, H, d] and V^T split
+//      as [B, H, d, Np] (Np = N rounded up to 4, zeros beyond N), so that
+//      every MMA operand is K-major;
+//   2. fused pass, one CTA per (b, h, 128-row Q tile), 6 warps:
+//        warp 0 lane 0   TMA: Qh, Ql once; Kh, Kl, V^Th, V^Tl of each 64-key
+//                        block into a 2-stage ring;
+//        warp 1 lane 0   MMAs: S = Qh Kh^T + Qh Kl^T + Ql Kh^T (fp32 in TMEM),
+//                        O += Ph Vh + Ph Vl + Pl Vh (P read from TMEM);
+//        warps 2-5       one thread per query row (TMEM lane): masked row max,
+//                        lazy rescale, P = 2^(s c - m) in float32 split into
+//                        Ph, Pl in TMEM; finally O / l and L.
+// TMEM: S [0, 64), Ph [64, 128), Pl [128, 192), O [192, 256).  S(j+1) is
+// computed while the softmax works on block j; PV(j) runs once P(j) is in
+// TMEM.  Every wait is bounded (FA_ERR_TIMEOUT, abort flag, drain).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cfloat>
+#include <cmath>
+#include <cstdint>
+
+#include "fa_common.cuh"
+#include "sm103_ptx.cuh"
+#include "tmap.h"
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;                  // query rows per CTA
+constexpr int kBN = 64;                   // keys per block
+constexpr int kDP = 64;                   // padded head dim (d <= 64)
+constexpr int kThreads = 192;
+constexpr int kStages = 2;
+constexpr int kQChunk = kBM * 128;        // 32 fp32 columns of 128 rows
+constexpr int kKChunk = kBN * 128;        // 32 fp32 columns of 64 rows
+constexpr int kQTile = 2 * kQChunk;       // 128 x 64 fp32
+constexpr int kKTile = 2 * kKChunk;       // 64 x 64 fp32
+constexpr int kOffQh = 0, kOffQl = kQTile;
+constexpr int kOffStage = 2 * kQTile;     // stage s: Kh, Kl, Vh, Vl
+constexpr int kStageBytes = 4 * kKTile;
+constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per block");
+constexpr int kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColPh = 64, kColPl = 128, kColO = 192;
+constexpr float kRescaleThreshold = 8.0f;
+
+// D[tmem] (+)= A * B with tf32 operands (32-bit elements, fp32 accumulate):
+// A from shared memory (SS) or TMEM (TS), B from shared memory.
+__device__ __forceinline__ void mma_ss_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor for kind::tf32: D format F32 (bits 4-5 = 1), A and B
+// format TF32 (code 2 in bits 7-9 and 10-12), both K-major, N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// 4-D float32 tensor map with the 128-byte swizzle (box inner extent 32
+// floats = 128 bytes); elements outside `dims` read as zero.
+cudaError_t make_f32_tmap(CUtensorMap* map, const void* base, const cuuint64_t dims[4],
+                          const cuuint64_t strides[3], const cuuint32_t box[4]) {
+  auto fn = encode_tiled_fn();
+  if (fn == nullptr) return cudaErrorSymbolNotFound;
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Nearest tf32 value (ties away from zero) of a finite float32 of magnitude
+// below 2^127: add half of the dropped 13-bit field, then clear it.
+__device__ __forceinline__ float tf32_rn(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
+
+// Split pass.  One thread per element of q, k, v ([B, N, H, d]); V^T rows of
+// one (b, h) are Np floats apart.  Threads with n in [N, Np) write the zero
+// padding of V^T.
+__global__ void __launch_bounds__(256) split_kernel(const float* q, const float* k, const float* v,
+                                                    float* qh, float* ql, float* kh, float* kl,
+                                                    float* vth, float* vtl, int B, int N, int H,
+                                                    int d, int Np) {
+  const size_t total = static_cast<size_t>(B) * Np * H * d;
+  for (size_t x = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < total;
+       x += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(x % d);
+    const size_t r = x / d;
+    const int h = static_cast<int>(r % H);
+    const size_t bn = r / H;
+    const int n = static_cast<int>(bn % Np);
+    const int b = static_cast<int>(bn / Np);
+    const size_t vt = ((static_cast<size_t>(b) * H + h) * d + c) * Np + n;
+    if (n >= N) {
+      vth[vt] = 0.0f;
+      vtl[vt] = 0.0f;
+      continue;
+    }
+    const size_t e = ((static_cast<size_t>(b) * N + n) * H + h) * d + c;
+    const float a = q[e], bk = k[e], bv = v[e];
+    const float ah = tf32_rn(a), bh = tf32_rn(bk), vh = tf32_rn(bv);
+    qh[e] = ah;
+    ql[e] = tf32_rn(a - ah);
+    kh[e] = bh;
+    kl[e] = tf32_rn(bk - bh);
+    vth[vt] = vh;
+    vtl[vt] = tf32_rn(bv - vh);
+  }
+}
+
+
+struct Tf32Bars {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full, s_free, p_full, pv_done, drain, probe;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void tf32_abort(Tf32Bars* bars, int* status) {
+  record_error(status, FA_ERR_TIMEOUT);
+  *reinterpret_cast<volatile int*>(&bars->abort) = 1;
+}
+
+// K-step offsets (8 tf32 = 32 bytes) inside a 2-chunk K-major tile, in the
+// descriptor's 16-byte units.
+__device__ __forceinline__ uint64_t kstep(int kk, int chunk_bytes) {
+  return static_cast<uint64_t>(((kk >> 2) * chunk_bytes + (kk & 3) * 32) >> 4);
+}
+
+template <bool kCausal>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tf32x3_kernel(const __grid_constant__ CUtensorMap tmQh,
+                      const __grid_constant__ CUtensorMap tmQl,
+                      const __grid_constant__ CUtensorMap tmKh,
+                      const __grid_constant__ CUtensorMap tmKl,
+                      const __grid_constant__ CUtensorMap tmVh,
+                      const __grid_constant__ CUtensorMap tmVl, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Tf32Bars* bars = reinterpret_cast<Tf32Bars*>(smem + kOffBar);
+  const volatile int* abort_flag = &bars->abort;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int N = p.N, H = p.H;
+  const int nq = (N + kBM - 1) / kBM, nk = (N + kBN - 1) / kBN;
+  const int qt = blockIdx.x % nq, bh = blockIdx.x / nq;
+  const int b = bh / H, h = bh % H;
+  // key blocks this tile visits (causal: up to its last row's diagonal)
+  const int nb = kCausal ? min(nk, (min(N, (qt + 1) * kBM) - 1) / kBN + 1) : nk;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, kBM);
+    mbar_init(&bars->p_full, kBM);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->probe, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  bool run = true;
+  if (p.probe_timeout) {
+    // self-test of the bounded-wait path: nothing ever arrives on `probe`
+    if (threadIdx.x == 0 && !mbar_wait(&bars->probe, 0, abort_flag, kProbeBudget))
+      tf32_abort(bars, p.status);
+    __syncthreads();
+    run = false;
+  }
+  uint8_t* sQh = smem + kOffQh;
+  uint8_t* sQl = smem + kOffQl;
+  auto stage = [&](int s) { return smem + kOffStage + s * kStageBytes; };
+
+  if (run && warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(&bars->q_full, 2 * kQTile);
+      for (int ch = 0; ch < 2; ++ch) {
+        tma_load_4d(sQh + ch * kQChunk, &tmQh, &bars->q_full, ch * 32, h, qt * kBM, b);
+        tma_load_4d(sQl + ch * kQChunk, &tmQl, &bars->q_full, ch * 32, h, qt * kBM, b);
+      }
+      int j = 0;
+      for (; j < nb; ++j) {
+        const int s = j % kStages, round = j / kStages;
+        if (round > 0 &&
+            !mbar_wait(&bars->kv_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = stage(s);
+        mbar_arrive_expect_tx(&bars->kv_full[s], kStageBytes);
+        for (int ch = 0; ch < 2; ++ch) {
+          tma_load_4d(st + 0 * kKTile + ch * kKChunk, &tmKh, &bars->kv_full[s], ch * 32, h,
+                      j * kBN, b);
+          tma_load_4d(st + 1 * kKTile + ch * kKChunk, &tmKl, &bars->kv_full[s], ch * 32, h,
+                      j * kBN, b);
+          tma_load_4d(st + 2 * kKTile + ch * kKChunk, &tmVh, &bars->kv_full[s],
+                      j * kBN + ch * 32, 0, h, b);
+          tma_load_4d(st + 3 * kKTile + ch * kKChunk, &tmVl, &bars->kv_full[s],
+                      j * kBN + ch * 32, 0, h, b);
+        }
+      }
+      if (!ok) tf32_abort(bars, p.status);
+      // every issued copy has landed before the CTA may exit
+      mbar_wait(&bars->q_full, 0, nullptr, kDrainBudget);
+      for (int x = max(0, j - kStages); x < j; ++x)
+        mbar_wait(&bars->kv_full[x % kStages], (x / kStages) & 1, nullptr, kDrainBudget);
+    }
+    __syncwarp();
+  }
+  else if (run && warp == 1) {
+    // ================ MMA issuer (whole warp waits, lane 0 issues) ================
+    const bool leader = lane == 0;
+    constexpr uint32_t kIdesc = idesc_tf32(kBM, kBN);   // S: N = 64 keys; PV: N = 64 columns
+    const int nks = p.d / 8;                            // K-steps over the head dim
+    const uint64_t dQh = sdesc_sw128(smem_u32(sQh), 16, 1024);
+    const uint64_t dQl = sdesc_sw128(smem_u32(sQl), 16, 1024);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, kWaitBudget));
+    auto pv_step = [&](int jj) -> bool {   // O += Ph Vh + Ph Vl + Pl Vh of block jj
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_full, jj & 1, abort_flag, kWaitBudget)))
+        return false;
+      tc_fence_after();
+      if (leader) {
+        uint8_t* st = stage(jj % kStages);
+        const uint64_t dVh = sdesc_sw128(smem_u32(st + 2 * kKTile), 16, 1024);
+        const uint64_t dVl = sdesc_sw128(smem_u32(st + 3 * kKTile), 16, 1024);
+        for (int kk = 0; kk < kBN / 8; ++kk)
+          mma_ts_tf32(tmem + kColO, tmem + kColPh + kk * 8, dVh + kstep(kk, kKChunk), kIdesc,
+                      (jj > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBN / 8; ++kk)
+          mma_ts_tf32(tmem + kColO, tmem + kColPh + kk * 8, dVl + kstep(kk, kKChunk), kIdesc, 1u);
+        for (int kk = 0; kk < kBN / 8; ++kk)
+          mma_ts_tf32(tmem + kColO, tmem + kColPl + kk * 8, dVh + kstep(kk, kKChunk), kIdesc, 1u);
+        mma_commit(&bars->pv_done);
+        mma_commit(&bars->kv_empty[jj % kStages]);   // S and PV of jj both read the stage
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int j = 0; j < nb && ok; ++j) {
+      const int s = j % kStages;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&bars->kv_full[s], (j / kStages) & 1, abort_flag, kWaitBudget) &&
+                          (j == 0 ||
+                           mbar_wait(&bars->s_free, (j - 1) & 1, abort_flag, kWaitBudget)))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (leader) {
+        uint8_t* st = stage(s);
+        const uint64_t dKh = sdesc_sw128(smem_u32(st), 16, 1024);
+        const uint64_t dKl = sdesc_sw128(smem_u32(st + kKTile), 16, 1024);
+        for (int kk = 0; kk < nks; ++kk)
+          mma_ss_tf32(tmem + kColS, dQh + kstep(kk, kQChunk), dKh + kstep(kk, kKChunk), kIdesc,
+                      kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < nks; ++kk)
+          mma_ss_tf32(tmem + kColS, dQh + kstep(kk, kQChunk), dKl + kstep(kk, kKChunk), kIdesc, 1u);
+        for (int kk = 0; kk < nks; ++kk)
+          mma_ss_tf32(tmem + kColS, dQl + kstep(kk, kQChunk), dKh + kstep(kk, kKChunk), kIdesc, 1u);
+        mma_commit(&bars->s_full);
+      }
+      __syncwarp();
+      if (j > 0 && !pv_step(j - 1)) ok = false;
+    }
+    if (ok && !pv_step(nb - 1)) ok = false;
+    if (!ok && leader) tf32_abort(bars, p.status);
+    // no MMA may be in flight when TMEM is released
+    mma_commit_w(&bars->drain, leader ? 1u : 0u);
+    mbar_wait(&bars->drain, 0, nullptr, kDrainBudget);
+    __syncwarp();
+  } else if (run && warp >= 2) {
+    // ======================= softmax / epilogue (warps 2-5) =======================
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
+    const int q_row = qt * kBM + row;
+    const float c = p.scale_log2;   // any sign: scores are scaled before the max
+    float m_ref = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, abort_flag, kWaitBudget))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[kBN];
+      tmem_ld32(tmem + lb + kColS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tmem + lb + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld_wait(sr);
+      tc_fence_before();
+      mbar_arrive(&bars->s_free);   // S may take the next block's scores
+      float t[kBN];
+#pragma unroll
+      for (int i = 0; i < kBN; ++i) t[i] = __uint_as_float(sr[i]) * c;
+      const int k0 = j * kBN;
+      if ((kCausal && k0 + kBN - 1 > qt * kBM) || k0 + kBN > N) {
+        const int lim = min(N - 1 - k0, kCausal ? q_row - k0 : kBN - 1);
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) t[i] = (i > lim) ? -INFINITY : t[i];
+      }
+      float m_blk = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kBN; ++i) m_blk = fmaxf(m_blk, t[i]);
+      // lazy rescale: move the reference max only when it rises enough
+      const bool rise = (m_ref == -INFINITY) ? (m_blk != -INFINITY)
+                                             : (m_blk > m_ref + kRescaleThreshold);
+      float alpha = 1.0f;
+      if (rise) {
+        alpha = (m_ref == -INFINITY) ? 0.0f : fast_exp2(m_ref - m_blk);
+        m_ref = m_blk;
+      }
+      l *= alpha;
+      const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+      uint32_t ph[kBN], pl[kBN];
+      float ls = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kBN; ++i) {
+        const float pv = fast_exp2(t[i] - m_use);
+        ls += pv;
+        const float hi = tf32_rn(pv);
+        ph[i] = __float_as_uint(hi);
+        pl[i] = __float_as_uint(tf32_rn(pv - hi));
+      }
+      l += ls;
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, rise);
+      // P and O are free once the previous block's PV has completed
+      if (j > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done, (j - 1) & 1, abort_flag, kWaitBudget))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (rescale) {
+#pragma unroll
+        for (int cc = 0; cc < kDP / 32; ++cc) {
+          uint32_t orr[32];
+          __syncwarp();
+          tmem_ld32(tmem + lb + kColO + cc * 32, orr);
+          tmem_ld_wait(orr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          tmem_st32(tmem + lb + kColO + cc * 32, orr);
+        }
+      }
+      __syncwarp();
+      tmem_st32(tmem + lb + kColPh, *reinterpret_cast<uint32_t(*)[32]>(&ph[0]));
+      tmem_st32(tmem + lb + kColPh + 32, *reinterpret_cast<uint32_t(*)[32]>(&ph[32]));
+      tmem_st32(tmem + lb + kColPl, *reinterpret_cast<uint32_t(*)[32]>(&pl[0]));
+      tmem_st32(tmem + lb + kColPl + 32, *reinterpret_cast<uint32_t(*)[32]>(&pl[32]));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+    }
+    if (ok && !__all_sync(0xffffffffu,
+                          mbar_wait(&bars->pv_done, (nb - 1) & 1, abort_flag, kWaitBudget)))
+      ok = false;
+    if (ok) {
+      // ---- epilogue: O / l in float32, L = (m + log2 l) ln 2 ----
+      tc_fence_after();
+      const bool live = l > 0.0f;
+      const float inv = live ? 1.0f / l : 0.0f;
+      const bool store = q_row < N;
+      float* orow = static_cast<float*>(p.o) +
+                    ((static_cast<size_t>(b) * N + (store ? q_row : 0)) * H + h) * p.d;
+#pragma unroll
+      for (int cc = 0; cc < kDP / 32; ++cc) {
+        uint32_t orr[32];
+        __syncwarp();
+        tmem_ld32(tmem + lb + kColO + cc * 32, orr);
+        tmem_ld_wait(orr);
+        if (store) {
+#pragma unroll
+          for (int qv = 0; qv < 8; ++qv) {
+            const int col = cc * 32 + qv * 4;
+            if (col < p.d)
+              *reinterpret_cast<float4*>(orow + col) =
+                  make_float4(__uint_as_float(orr[qv * 4 + 0]) * inv,
+                              __uint_as_float(orr[qv * 4 + 1]) * inv,
+                              __uint_as_float(orr[qv * 4 + 2]) * inv,
+                              __uint_as_float(orr[qv * 4 + 3]) * inv);
+          }
+        }
+      }
+      if (store)
+        p.lse[(static_cast<size_t>(b) * H + h) * N + q_row] =
+            live ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    } else {
+      tf32_abort(bars, p.status);
+    }
+    tc_fence_before();
+  }
+
+  // ---- teardown ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+}  // namespace fa
+
+namespace fa {
+namespace {
+
+int round4(int n) { return (n + 3) & ~3; }
+
+}  // namespace
+
+// Workspace: Qh, Ql, Kh, Kl ([B, N, H, d] float32 each), V^Th, V^Tl
+// ([B, H, d, Np] float32 each), each part rounded up to 256 bytes.
+size_t tf32x3_workspace_bytes(int B, int H, int N, int d) {
+  const size_t a = (static_cast<size_t>(B) * N * H * d * 4 + 255) & ~static_cast<size_t>(255);
+  const size_t t =
+      (static_cast<size_t>(B) * H * d * round4(N) * 4 + 255) & ~static_cast<size_t>(255);
+  return 4 * a + 2 * t;
+}
+
+cudaError_t launch_fwd_tf32x3(const FwdParams& p, void* workspace, cudaStream_t st, bool causal) {
+  const int B = p.B, H = p.H, N = p.N, d = p.d, Np = round4(N);
+  if (d > kDP || d % 8 != 0) return cudaErrorNotSupported;
+  const size_t a = (static_cast<size_t>(B) * N * H * d * 4 + 255) & ~static_cast<size_t>(255);
+  const size_t t = (static_cast<size_t>(B) * H * d * Np * 4 + 255) & ~static_cast<size_t>(255);
+  char* w = static_cast<char*>(workspace);
+  float *qh = reinterpret_cast<float*>(w), *ql = reinterpret_cast<float*>(w + a),
+        *kh = reinterpret_cast<float*>(w + 2 * a), *kl = reinterpret_cast<float*>(w + 3 * a),
+        *vth = reinterpret_cast<float*>(w + 4 * a), *vtl = reinterpret_cast<float*>(w + 4 * a + t);
+  // tensor maps: [B, N, H, d] as (d, H, N, B); V^T [B, H, d, Np] as (Np, d, H, B)
+  const cuuint64_t dq[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                            static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+  const cuuint64_t sq[3] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(H) * d * 4,
+                            static_cast<cuuint64_t>(N) * H * d * 4};
+  const cuuint64_t dv[4] = {static_cast<cuuint64_t>(Np), static_cast<cuuint64_t>(d),
+                            static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t sv[3] = {static_cast<cuuint64_t>(Np) * 4, static_cast<cuuint64_t>(d) * Np * 4,
+                            static_cast<cuuint64_t>(H) * d * Np * 4};
+  const cuuint32_t box_q[4] = {32u, 1u, static_cast<cuuint32_t>(kBM), 1u};
+  const cuuint32_t box_k[4] = {32u, 1u, static_cast<cuuint32_t>(kBN), 1u};
+  const cuuint32_t box_v[4] = {32u, static_cast<cuuint32_t>(kDP), 1u, 1u};
+  CUtensorMap mqh, mql, mkh, mkl, mvh, mvl;
+  cudaError_t e = make_f32_tmap(&mqh, qh, dq, sq, box_q);
+  if (e == cudaSuccess) e = make_f32_tmap(&mql, ql, dq, sq, box_q);
+  if (e == cudaSuccess) e = make_f32_tmap(&mkh, kh, dq, sq, box_k);
+  if (e == cudaSuccess) e = make_f32_tmap(&mkl, kl, dq, sq, box_k);
+  if (e == cudaSuccess) e = make_f32_tmap(&mvh, vth, dv, sv, box_v);
+  if (e == cudaSuccess) e = make_f32_tmap(&mvl, vtl, dv, sv, box_v);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return cudaErrorInvalidDevice;
+  const size_t total = static_cast<size_t>(B) * Np * H * d;
+  const size_t want = (total + 255) / 256, cap = static_cast<size_t>(sms) * 8;
+  split_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
+      static_cast<const float*>(p.q), static_cast<const float*>(p.k),
+      static_cast<const float*>(p.v), qh, ql, kh, kl, vth, vtl, B, N, H, d, Np);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long ctas = static_cast<long long>(B) * H * ((N + kBM - 1) / kBM);
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  auto kern = causal ? fwd_tf32x3_kernel<true> : fwd_tf32x3_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  FwdParams pc = p;
+  void* args[] = {&mqh, &mql, &mkh, &mkl, &mvh, &mvl, &pc};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(static_cast<unsigned>(ctas)),
+                          dim3(kThreads), args, kSmemBytes, st);
+}
+
+}  // namespace fa

@@ -320,6 +320,32 @@ fa_status fa_fwd_unfused(const void* q, const void* k, const void* v, void* o, f
                          fa_dtype dtype, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/*
+ * fa_fwd_tf32x3 — float32 forward on the tensor cores.
+ *
+ * Same operation and outputs as fa_fwd with FA_DTYPE_F32 ("Flash Attention 2
+ * — forward pass notes", sections "Loop (per (b, h, Q-tile))" and "What's
+ * still needed for full FA2" item 1), computed with tcgen05 kind::tf32
+ * products instead of the float32 FMA pipes.  Every float32 input x is
+ * split into hi (x rounded to tf32) and lo (x - hi rounded to tf32), and each
+ * product is taken as hi*hi + hi*lo + lo*hi (3xTF32), in Q K^T and in P V
+ * alike; accumulation, the softmax and the outputs are float32.  The
+ * relative error per product is at most about 3 * 2^-22.  Inputs must be
+ * finite with |x| < 2^127.
+ *
+ *   q, k, v   in : [B, N, H, d] float32
+ *   o        out : [B, N, H, d] float32;  lse out : [B, H, N] float32
+ *   d            : a multiple of 8 in [8, 64] (d > 64: FA_ERR_UNSUPPORTED)
+ *   workspace    : DEVICE, 256-byte aligned, >= fa_fwd_tf32x3_workspace_size
+ *                  (B, H, N, d) bytes: the hi/lo split of q, k and v (v
+ *                  transposed per head), 6 float32 copies of an input
+ *   other arguments as in fa_fwd.
+ */
+size_t fa_fwd_tf32x3_workspace_size(int B, int H, int N, int d);
+fa_status fa_fwd_tf32x3(const float* q, const float* k, const float* v, float* o, float* lse,
+                        int B, int H, int N, int d, float scale, int causal,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* fa_status_string — static, human-readable name of a status code. */
 const char* fa_status_string(fa_status s);
 

@@ -219,3 +219,27 @@ def test_unfused_rejects_invalid_arguments(lib, kw, want):
              stream=None)
     a.update(kw)
     assert _lib.fa_fwd_unfused(**a) == want
+
+
+def test_tf32x3_workspace_size(lib):
+    from exact_attention_fwd_gb300 import _lib
+    # 4 split copies of [1, 10, 2, 8] floats (640 -> 768 bytes each) and 2 of
+    # V^T [1, 2, 8, 12] floats (768 bytes each)
+    assert _lib.fa_fwd_tf32x3_workspace_size(1, 2, 10, 8) == 4 * 768 + 2 * 768
+    assert _lib.fa_fwd_tf32x3_workspace_size(1, 2, 0, 8) == 0
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), 1), (dict(workspace=0), 1),
+    (dict(d=72), 2), (dict(d=136), 2), (dict(d=12), 1),
+    (dict(workspace_bytes=100), 1),
+    (dict(workspace=16 * FAKE + 64), 1),
+    (dict(o=FAKE), 1),                     # aliases q
+    (dict(scale=float("nan")), 1),
+])
+def test_tf32x3_rejects_invalid_arguments(lib, kw, want):
+    from exact_attention_fwd_gb300 import _lib
+    a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, B=1, H=1, N=16, d=64,
+             scale=0.125, causal=1, workspace=16 * FAKE, workspace_bytes=1 << 22, stream=None)
+    a.update(kw)
+    assert _lib.fa_fwd_tf32x3(**a) == want
