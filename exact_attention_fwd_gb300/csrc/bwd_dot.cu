@@ -4,9 +4,13 @@
 // compute D once into a [B, H, N] buffer).
 //
 // Memory-bound: it reads O and dO once and writes 4 bytes per row.  Rows of
-// [B, N, H, d] tensors with consecutive (n, h) are contiguous, so a warp takes
-// 32 consecutive flattened rows and its lanes read consecutive 16-byte chunks
-// of them: every load instruction of the warp is one contiguous 512-byte span.
+// [B, N, H, d] tensors with consecutive (n, h) are contiguous, so the lanes of
+// a warp read consecutive 16-byte chunks of consecutive rows: every load
+// instruction of the warp is one contiguous 512-byte span.  When a row is a
+// power-of-two number of chunks (d = 8, 16, 32, 64, 128), each row belongs to
+// a fixed group of lanes, the row's partial dot products are summed with warp
+// shuffles, and every lane keeps 4 rows' chunks of both tensors in flight;
+// other head sizes stage the partial sums in shared memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -94,6 +98,63 @@ __global__ void __launch_bounds__(kThreads) dot_do_o_kernel(BwdParams p) {
   }
 }
 
+// Row = kCpr lanes (kCpr 16-byte chunks); a warp covers 32 / kCpr rows per
+// pass and kUnroll passes per iteration.
+template <int kElt, int kCpr>
+__global__ void __launch_bounds__(kThreads) dot_shfl_kernel(BwdParams p) {
+  constexpr int kRowsPass = 32 / kCpr;
+  constexpr int kUnroll = 4;
+  constexpr int kRowsIter = kRowsPass * kUnroll;
+  const int lane = threadIdx.x & 31, sub = lane % kCpr, rr = lane / kCpr;
+  const long long rows = static_cast<long long>(p.B) * p.N * p.H;
+  const uint4* O = static_cast<const uint4*>(p.o);
+  const uint4* G = static_cast<const uint4*>(p.dO);
+  const long long w0 = static_cast<long long>(blockIdx.x) * (kThreads / 32) + threadIdx.x / 32;
+  const long long nw = static_cast<long long>(gridDim.x) * (kThreads / 32);
+  for (long long r0 = w0 * kRowsIter; r0 < rows; r0 += nw * kRowsIter) {
+    uint4 a[kUnroll], b[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long r = r0 + u * kRowsPass + rr;
+      if (r < rows) {
+        a[u] = __ldg(O + r * kCpr + sub);
+        b[u] = __ldg(G + r * kCpr + sub);
+      } else {
+        a[u] = make_uint4(0u, 0u, 0u, 0u);
+        b[u] = a[u];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      float s = dot_chunk<kElt>(a[u], b[u]);
+#pragma unroll
+      for (int off = kCpr / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      const long long r = r0 + u * kRowsPass + rr;
+      if (sub == 0 && r < rows) {
+        // flattened row r = (b * N + n) * H + h  ->  D[(b * H + h) * N + n]
+        const int h = static_cast<int>(r % p.H);
+        const long long bn = r / p.H;
+        const int n = static_cast<int>(bn % p.N);
+        const long long bb = bn / p.N;
+        p.D[(bb * p.H + h) * p.N + n] = s;
+      }
+    }
+  }
+}
+
+template <int kElt>
+const void* dot_kernel_for(int cpr) {
+  switch (cpr) {
+    case 1: return reinterpret_cast<const void*>(dot_shfl_kernel<kElt, 1>);
+    case 2: return reinterpret_cast<const void*>(dot_shfl_kernel<kElt, 2>);
+    case 4: return reinterpret_cast<const void*>(dot_shfl_kernel<kElt, 4>);
+    case 8: return reinterpret_cast<const void*>(dot_shfl_kernel<kElt, 8>);
+    case 16: return reinterpret_cast<const void*>(dot_shfl_kernel<kElt, 16>);
+    case 32: return reinterpret_cast<const void*>(dot_shfl_kernel<kElt, 32>);
+    default: return reinterpret_cast<const void*>(dot_do_o_kernel<kElt>);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_dot(const BwdParams& p, int elt, cudaStream_t s) {
@@ -107,9 +168,10 @@ cudaError_t launch_bwd_dot(const BwdParams& p, int elt, cudaStream_t s) {
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   void* args[] = {const_cast<BwdParams*>(&p)};
-  const void* kern = elt == 2   ? reinterpret_cast<const void*>(dot_do_o_kernel<2>)
-                     : elt == 1 ? reinterpret_cast<const void*>(dot_do_o_kernel<1>)
-                                : reinterpret_cast<const void*>(dot_do_o_kernel<0>);
+  const int cpr = p.d * (elt == 0 ? 4 : 2) / 16;   // 16-byte chunks per row
+  const void* kern = elt == 2   ? dot_kernel_for<2>(cpr)
+                     : elt == 1 ? dot_kernel_for<1>(cpr)
+                                : dot_kernel_for<0>(cpr);
   return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), args, 0, s);
 }
 
