@@ -109,12 +109,6 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Named barrier over `nthreads` threads (a multiple of 32); id 0 is the one
-// __syncthreads uses.
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // ----------------------------------------------------------------------------
 // tcgen05: tensor memory
 // ----------------------------------------------------------------------------
@@ -341,8 +335,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ int elect_lane0() { return (threadIdx.x & 31) == 0; }
-
 // Per-warpgroup register budget changes (all 128 threads of the warpgroup).
 template <int N>
 __device__ __forceinline__ void regs_inc() {
@@ -361,13 +353,13 @@ __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   return d;
 }
 __device__ __forceinline__ float f2_lo(uint64_t x) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  float lo;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0, t}, %1;\n\t}" : "=f"(lo) : "l"(x));
   return lo;
 }
 __device__ __forceinline__ float f2_hi(uint64_t x) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  float hi;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {t, %0}, %1;\n\t}" : "=f"(hi) : "l"(x));
   return hi;
 }
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
@@ -388,11 +380,6 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float fmin3(float a, float b, float c) {
-  float d;
-  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
