@@ -279,6 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmG1, const __grid_constant__ CUtensorMap tmG2,
                   const BwdParams p) {
   using Cfg = BwdCfg<DP>;
+  // S/dP, acc1 and acc2 from three issuing warps (1, 3, 2): the causal dQ
+  // kernel only; elsewhere the third issuer's state pushes the 88-register
+  // helper warps into spills, and warp 1 issues S/dP and acc1
+  constexpr bool kThree = Cfg::kWide && !kDkDv && kCausal;
   constexpr int S = Cfg::kStages;
   constexpr int kBlk = Cfg::kBlk;
   constexpr bool kWide = Cfg::kWide;
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->acc_free, 256);
     mbar_init(&bars->dsum, 256);
     mbar_init(&bars->epi_staged, 256);
-    mbar_init(&bars->drain, kWide ? 2 : 1);
+    mbar_init(&bars->drain, kThree ? 3 : (kWide ? 2 : 1));   // one commit per MMA warp
     mbar_init(&bars->probe, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -424,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bars->r_full[x % Cfg::kRBufs], (x / Cfg::kRBufs) & 1, nullptr, kDrainBudget);
     }
     __syncwarp();
-  } else if (run && (warp == 1 || (kWide && warp == 2))) {
+  } else if (run && (warp == 1 || (kWide && warp == 2) || (kThree && warp == 3))) {
     // ============ MMA issuers (whole warp waits, lane 0 issues) ============
     const uint32_t leader = (lane == 0) ? 1u : 0u;
     constexpr uint32_t kIdescSP = idesc16<kF16>(kRows, kBlk, false, false);
@@ -501,10 +505,78 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
       const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
+      if (kThree && warp == 3) {
+        // third MMA warp (causal dQ kernel): the acc1 accumulations of every block.
+        // Before waiting for a block's P and dS it prepares the next block:
+        // the per-query -L2 and -D (dK/dV) or the second half of the fp16
+        // copy of C1 (dQ), so the element-wise warps do not wait for them.
+        // S/dP (warp 1), acc1 (warp 3) and acc2 (warp 2) come from three
+        // threads, so no chain of MMAs waits behind another in program order.
+        const size_t hb = (static_cast<size_t>(w.b) * H + w.h) * N;
+        auto prep = [&](int t) -> bool {
+          const int cb = c + t, s = cb % S;
+          if constexpr (kDkDv) {
+            float nl2[kBlk / 32], nd[kBlk / 32];
+#pragma unroll
+            for (int u = 0; u < kBlk / 32; ++u) {
+              const int q = (w.i0 + t) * kBlk + u * 32 + lane;
+              float l2 = INFINITY, dd = 0.0f;   // padded or fully masked query: P = 0
+              if (q < N) {
+                const float L = p.lse[hb + q];
+                if (L != -INFINITY) {
+                  l2 = L * kLog2e;
+                  dd = p.D[hb + q];
+                }
+              }
+              nl2[u] = -l2;   // stored negated: the exponent is s c + (-L2)
+              nd[u] = -dd;
+            }
+            if (!wait_c(cb)) return false;
+            float* vec = stage_vec(s);
+#pragma unroll
+            for (int u = 0; u < kBlk / 32; ++u) {
+              vec[u * 32 + lane] = nl2[u];
+              vec[kBlk + u * 32 + lane] = nd[u];
+            }
+            mbar_arrive(&bars->vec_full[s]);
+          } else {
+            if (!wait_c(cb)) return false;
+            if (!kF16) {
+              convert_c1(s, kVecs / 2, kVecs, lane, 32);
+              mbar_arrive(&bars->conv_full[s]);
+            }
+          }
+          return true;
+        };
+        if (w.nb > 0 && !prep(0)) {
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < w.nb; ++t) {
+          const int cb = c + t;
+          if (t + 1 < w.nb && !prep(t + 1)) {
+            ok = false;
+            break;
+          }
+          if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
+              !wait_acc_inputs(cb, t == 0, li, !kDkDv)) {
+            ok = false;
+            break;
+          }
+          ++npd;
+          tc_fence_after();
+          issue_acc(cb, t == 0, Cfg::kTP, Cfg::kTdS, 1);
+          mma_commit_w(&bars->acc_done, leader);
+          if (t == w.nb - 1) mma_commit_w(&bars->acc_full, leader);
+        }
+        c += w.nb;
+        continue;
+      }
       if (kWide && warp == 2) {
         // second MMA warp (wide layout): the acc2 accumulations of every
-        // block, concurrently with warp 1's acc1 ones (a single issuing
-        // thread cannot keep the tensor pipe busy with N = 64 MMAs)
+        // block, concurrently with the acc1 ones (warp 3 with kThree, else
+        // warp 1; a single issuing thread cannot keep the tensor pipe busy
+        // with N = 64 MMAs)
         for (int t = 0; t < w.nb; ++t) {
           const int cb = c + t;
           if (!kDkDv) {   // dQ: first half of the block's fp16 copy (warp 3 the second)
@@ -547,25 +619,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nsp;
           return true;
         };
-        if (!next_sp(c)) { ok = false; break; }
-        for (int t = 0; t < w.nb; ++t) {
-          const int cb = c + t;
-          if (t + 1 < w.nb) {
-            if (!next_sp(cb + 1)) { ok = false; break; }
-          } else {
-            // (wide layout: the epilogue releases the row buffer, which it
-            // uses as the staging tile of the gradient stores)
+        if constexpr (kThree) {
+          // S/dP only, each block's as soon as the element-wise warps hold
+          // the previous one in registers (warp 3 issues acc1)
+          for (int t = 0; t < w.nb && ok; ++t)
+            if (!next_sp(c + t)) ok = false;
+          if (!ok) break;
+        } else {
+          // S/dP of the next block, then acc1 of this one
+          if (!next_sp(c)) { ok = false; break; }
+          for (int t = 0; t < w.nb; ++t) {
+            const int cb = c + t;
+            if (t + 1 < w.nb && !next_sp(cb + 1)) { ok = false; break; }
+            if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
+                !wait_acc_inputs(cb, t == 0, li, !kDkDv)) {
+              ok = false;
+              break;
+            }
+            ++npd;
+            tc_fence_after();
+            issue_acc(cb, t == 0, Cfg::kTP, Cfg::kTdS, 1);
+            mma_commit_w(&bars->acc_done, leader);
+            if (t == w.nb - 1) mma_commit_w(&bars->acc_full, leader);
           }
-          if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
-              !wait_acc_inputs(cb, t == 0, li, !kDkDv)) {
-            ok = false;
-            break;
-          }
-          ++npd;
-          tc_fence_after();
-          issue_acc(cb, t == 0, Cfg::kTP, Cfg::kTdS, 1);
-          mma_commit_w(&bars->acc_done, leader);
-          if (t == w.nb - 1) mma_commit_w(&bars->acc_full, leader);
         }
       } else {
         // narrow: S/dP of global block cb go to buffer cb & 1; warpgroup cb & 1
@@ -637,10 +713,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (run && warp == 3) {
     // ============ fp16 copy of each streamed C1 tile (same swizzled layout) ============
-    // Narrow layout: the whole copy.  dQ, wide: the second half (warp 2 makes
-    // the first).  dK/dV, wide: no copy (the element-wise warps make it), but
-    // the per-query -L2 and -D of each block (read from global memory before
-    // the block has landed).
+    // Narrow layout: the whole copy.  dK/dV, wide: no copy (the element-wise
+    // warps make it), but the per-query -L2 and -D of each block (read from
+    // global memory before the block has landed).  dQ, wide: the second half
+    // (warp 2 makes the first); with kThree warp 3 is the third MMA issuer
+    // and makes that half there.
     constexpr bool kVec = kWide && kDkDv;
     int c = 0, li = 0;
     bool ok = true;
