@@ -148,3 +148,24 @@ def test_merge_rows_without_contribution():
     mask[1, 0] = False
     assert (o[0][mask] == 0.0).all()
     assert np.isneginf(lse[0].T[mask]).all()
+
+
+def test_partial_bounded_wait_self_test():
+    """The split-KV pass runs the forward kernel in split mode: the self-test
+    switch makes its first wait time out and report FA_ERR_TIMEOUT."""
+    import os
+    torch = require_gpu()
+    from exact_attention_fwd_gb300 import _lib, api
+    inp = make(1, 2, 600, 64, "bf16", 13800)
+    q, k, v = _qkv(inp)
+    os.environ["FA_SELFTEST_WAIT_TIMEOUT"] = "1"
+    try:
+        api.forward_partial(q, k, v, 256, causal=True)
+        st = api.sync_status()
+    finally:
+        del os.environ["FA_SELFTEST_WAIT_TIMEOUT"]
+    assert st == _lib.FA_ERR_TIMEOUT
+    assert api.sync_status() == 0
+    o, lse = api.forward_splitkv(q, k, v, 2, causal=True)
+    assert api.sync_status() == 0
+    compare_fwd(inp, o, lse, True, default_scale(64))

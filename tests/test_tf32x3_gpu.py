@@ -64,3 +64,25 @@ def test_unusual_scales_tf32x3(scale):
     for causal in (False, True):
         o, lse = _run(inp, causal, scale)
         compare_fwd(inp, o, lse, causal, scale)
+
+
+def test_tf32x3_bounded_wait_self_test():
+    """The self-test switch makes the kernel's first wait time out: FA_ERR_TIMEOUT
+    through the status word, the context stays usable."""
+    import os
+    torch = require_gpu()
+    from exact_attention_fwd_gb300 import _lib, api
+    inp = make(1, 2, 256, 64, "f32", 16700)
+    dev = torch.device("cuda", 0)
+    q, k, v = (inp.torch(t, dev) for t in ("q", "k", "v"))
+    os.environ["FA_SELFTEST_WAIT_TIMEOUT"] = "1"
+    try:
+        api.forward_tf32x3(q, k, v, causal=True)
+        st = api.sync_status()
+    finally:
+        del os.environ["FA_SELFTEST_WAIT_TIMEOUT"]
+    assert st == _lib.FA_ERR_TIMEOUT
+    assert api.sync_status() == 0
+    o, lse = api.forward_tf32x3(q, k, v, causal=True)
+    assert api.sync_status() == 0
+    compare_fwd(inp, o, lse, True, default_scale(64))
