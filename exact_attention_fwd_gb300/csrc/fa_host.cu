@@ -1,7 +1,8 @@
 // fa_host.cu — forward + backward on HOST buffers, pipelined over batch chunks.
 //
-// The batch is cut into chunks of `batch_chunk` sequences (every tensor is
-// [B, ...] with B outermost, so a chunk is one contiguous slab per tensor).
+// The batch is cut into chunks of up to `batch_chunk` sequences (every tensor
+// is [B, ...] with B outermost, so a chunk is one contiguous slab per tensor);
+// the first and last chunks are smaller (see ChunkPlan).
 // Two device slots in the caller's workspace alternate: while chunk c is being
 // computed, chunk c+1's inputs are copied in and chunk c-1's results copied
 // out.  Three streams carry the work:
@@ -71,6 +72,32 @@ fa_status copy_streams(cudaStream_t* h2d, cudaStream_t* d2h) {
   return FA_OK;
 }
 
+// Chunk sizes: bc/4 and bc/2 first, bc/2 and bc/4 last, full chunks between,
+// so that the copy-in before the first kernels and the kernels and copy-out
+// after the last copy-in (the parts nothing overlaps) are short.  Batches too
+// small for the ramp use full chunks.
+struct ChunkPlan {
+  int bc, q, h, mid, nmid, n;   // mid: sequences in the full-size part
+  bool ramp;
+  ChunkPlan(int B, int bc_) : bc(bc_) {
+    q = bc / 4 > 0 ? bc / 4 : 1;
+    h = bc / 2 > 0 ? bc / 2 : 1;
+    ramp = bc >= 4 && B >= 2 * (q + h) + bc;
+    mid = ramp ? B - 2 * (q + h) : B;
+    nmid = (mid + bc - 1) / bc;
+    n = nmid + (ramp ? 4 : 0);
+  }
+  int size(int c) const {
+    if (ramp) {
+      if (c == 0 || c == n - 1) return q;
+      if (c == 1 || c == n - 2) return h;
+      c -= 2;
+    }
+    const int left = mid - c * bc;
+    return left < bc ? left : bc;
+  }
+};
+
 const char* cbyte(const void* p) { return static_cast<const char*>(p); }
 char* byte(void* p) { return static_cast<char*>(p); }
 
@@ -135,11 +162,12 @@ fa_status fa_fwd_bwd_host(const void* q, const void* k, const void* v, const voi
   ok(cudaStreamWaitEvent(hs, ev_start, 0));
   ok(cudaStreamWaitEvent(ds, ev_start, 0));
 
-  const int nchunks = (B + bc - 1) / bc;
+  const ChunkPlan plan(B, bc);
   bool used[2] = {false, false};
-  for (int c = 0; c < nchunks && st == FA_OK; ++c) {
+  int b0 = 0;
+  for (int c = 0; c < plan.n && st == FA_OK; b0 += plan.size(c), ++c) {
     const int s = c & 1;
-    const int b0 = c * bc, nb = (B - b0 < bc) ? (B - b0) : bc;
+    const int nb = plan.size(c);
     char* slot = byte(workspace) + static_cast<size_t>(s) * L.total;
     const size_t in_b = nb * seq_in, gr_b = nb * seq_grad, rw_b = nb * seq_rows;
     const size_t hin = static_cast<size_t>(b0) * seq_in, hgr = static_cast<size_t>(b0) * seq_grad,

@@ -17,7 +17,7 @@ def _host(inp, t, pin=True):
     return x.pin_memory() if pin else x
 
 
-@pytest.mark.parametrize("B,chunk", [(5, 2), (4, 4), (3, 8), (6, 1)])
+@pytest.mark.parametrize("B,chunk", [(5, 2), (4, 4), (3, 8), (6, 1), (13, 4)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_host_equals_device_calls(B, chunk, causal):
     torch = require_gpu()
