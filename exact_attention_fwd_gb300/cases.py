@@ -1,0 +1,122 @@
+"""Named single-GPU workloads for timing and profiling the entry points.
+
+``python -m exact_attention_fwd_gb300.cases <name> [--reps R]`` builds seeded
+N(0, 1) inputs on ``cuda:0``, makes one untimed call, then times ``R`` calls
+with CUDA events and prints one line: the case, its shape and the mean time
+per call.  The captures in ``profiles/`` name these cases, so every profile
+can be re-run from the committed tree.  The first call is the warm-up, so an
+``ncu -s 1 -c 1`` capture of a one-kernel case takes a warm launch.
+
+Cases (FLOP counted as 4 B H d times the visible (query, key) pairs for a
+forward):
+
+* ``long_fwd``: B1 H32 N8192 d128 causal bf16, ``forward``;
+* ``gpt2_unfused``: B8 H16 N1024 d64 causal bf16, ``forward`` then
+  ``forward_unfused`` per repetition;
+* ``tf32x3``: B8 H16 N1024 d64 causal float32, ``forward_tf32x3`` (split pass
+  plus one tensor-core kernel);
+* ``splitkv``: B1 H1 N32768 d128 causal bf16, ``forward_splitkv`` with 8 key
+  slices (partial forward plus merge).
+"""
+import argparse
+
+import torch
+
+from . import api
+
+
+def _pairs(N, causal):
+    return N * (N + 1) // 2 if causal else N * N
+
+
+def _inputs(shape, dtype, dev, seed=0, count=3):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    return [torch.randn(*shape, device=dev, generator=g).to(dtype) for _ in range(count)]
+
+
+def _case_long_fwd(dev):
+    B, H, N, d = 1, 32, 8192, 128
+    q, k, v = _inputs((B, N, H, d), torch.bfloat16, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device=dev)
+    return (B, H, N, d), 4.0 * B * H * d * _pairs(N, True), \
+        lambda: api.forward(q, k, v, causal=True, out=o, lse=lse)
+
+
+def _case_gpt2_unfused(dev):
+    B, H, N, d = 8, 16, 1024, 64
+    q, k, v = _inputs((B, N, H, d), torch.bfloat16, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device=dev)
+    o2 = torch.empty_like(q)
+    lse2 = torch.empty(B, H, N, device=dev)
+    ws = api.unfused_workspace(B, H, N, d, dev)
+
+    def run():
+        api.forward(q, k, v, causal=True, out=o, lse=lse)
+        api.forward_unfused(q, k, v, causal=True, out=o2, lse=lse2, ws=ws)
+    return (B, H, N, d), 2 * 4.0 * B * H * d * _pairs(N, True), run
+
+
+def _case_tf32x3(dev):
+    B, H, N, d = 8, 16, 1024, 64
+    q, k, v = _inputs((B, N, H, d), torch.float32, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device=dev)
+    ws = torch.empty(api._lib.fa_fwd_tf32x3_workspace_size(B, H, N, d), dtype=torch.uint8,
+                     device=dev)
+    return (B, H, N, d), 4.0 * B * H * d * _pairs(N, True), \
+        lambda: api.forward_tf32x3(q, k, v, causal=True, out=o, lse=lse, ws=ws)
+
+
+def _case_splitkv(dev):
+    B, H, N, d, S = 1, 1, 32768, 128, 8
+    q, k, v = _inputs((B, N, H, d), torch.bfloat16, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device=dev)
+    ws = api.splitkv_workspace(B, H, N, d, S, dev)
+    return (B, H, N, d), 4.0 * B * H * d * _pairs(N, True), \
+        lambda: api.forward_splitkv(q, k, v, S, causal=True, out=o, lse=lse, ws=ws)
+
+
+CASES = {
+    "long_fwd": _case_long_fwd,
+    "gpt2_unfused": _case_gpt2_unfused,
+    "tf32x3": _case_tf32x3,
+    "splitkv": _case_splitkv,
+}
+
+
+def run_case(name, reps=5):
+    """Run case ``name`` once untimed and ``reps`` times timed; returns
+    (shape, mean milliseconds per call, TFLOP/s)."""
+    dev = torch.device("cuda", 0)
+    shape, flop, fn = CASES[name](dev)
+    fn()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(reps):
+        fn()
+    end.record()
+    end.synchronize()
+    status = api.sync_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after case {name}")
+    ms = start.elapsed_time(end) / reps
+    return shape, ms, flop / (ms * 1e-3) / 1e12
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("case", choices=sorted(CASES))
+    ap.add_argument("--reps", type=int, default=5)
+    a = ap.parse_args()
+    (B, H, N, d), ms, tf = run_case(a.case, a.reps)
+    print(f"{a.case} B{B} H{H} N{N} d{d}: {ms * 1e3:.1f} us per call, {tf:.1f} TFLOP/s")
+
+
+if __name__ == "__main__":
+    main()

@@ -13,9 +13,10 @@
 // are already tf32 values, so how the tensor cores reduce 32-bit operands to
 // tf32 does not matter.
 //
-//   1. split pass (HBM-bound): Qh, Ql, Kh, Kl as [B, N, H, d] and V^T split
-//      as [B, H, d, Np] (Np = N rounded up to 4, zeros beyond N), so that
-//      every MMA operand is K-major;
+//   1. split pass (HBM-bound): Qh, Ql, Kh, Kl as [B, N, H, d] (16-byte
+//      accesses) and V^T split as [B, H, d, Np] (Np = N rounded up to 4, zeros
+//      beyond N; transposed through shared-memory tiles), so that every MMA
+//      operand is K-major;
 //   2. fused pass, one CTA per (b, h, 128-row Q tile), 6 warps:
 //        warp 0 lane 0   TMA: Qh, Ql once; Kh, Kl, V^Th, V^Tl of each 64-key
 //                        block into a 2-stage ring;
@@ -109,37 +110,48 @@ __device__ __forceinline__ float tf32_rn(float x) {
   return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
-// Split pass.  One thread per element of q, k, v ([B, N, H, d]); V^T rows of
-// one (b, h) are Np floats apart.  Threads with n in [N, Np) write the zero
-// padding of V^T.
-__global__ void __launch_bounds__(256) split_kernel(const float* q, const float* k, const float* v,
-                                                    float* qh, float* ql, float* kh, float* kl,
-                                                    float* vth, float* vtl, int B, int N, int H,
-                                                    int d, int Np) {
-  const size_t total = static_cast<size_t>(B) * Np * H * d;
-  for (size_t x = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < total;
+// Split pass, Q and K: 4 elements per thread with 16-byte loads and stores.
+__global__ void __launch_bounds__(256) split_qk_kernel(const float4* q, const float4* k,
+                                                       float4* qh, float4* ql, float4* kh,
+                                                       float4* kl, size_t n4) {
+  for (size_t x = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < n4;
        x += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(x % d);
-    const size_t r = x / d;
-    const int h = static_cast<int>(r % H);
-    const size_t bn = r / H;
-    const int n = static_cast<int>(bn % Np);
-    const int b = static_cast<int>(bn / Np);
-    const size_t vt = ((static_cast<size_t>(b) * H + h) * d + c) * Np + n;
-    if (n >= N) {
-      vth[vt] = 0.0f;
-      vtl[vt] = 0.0f;
-      continue;
+    const float4 a = q[x], bk = k[x];
+    const float4 ah = make_float4(tf32_rn(a.x), tf32_rn(a.y), tf32_rn(a.z), tf32_rn(a.w));
+    const float4 bh = make_float4(tf32_rn(bk.x), tf32_rn(bk.y), tf32_rn(bk.z), tf32_rn(bk.w));
+    qh[x] = ah;
+    ql[x] = make_float4(tf32_rn(a.x - ah.x), tf32_rn(a.y - ah.y), tf32_rn(a.z - ah.z),
+                        tf32_rn(a.w - ah.w));
+    kh[x] = bh;
+    kl[x] = make_float4(tf32_rn(bk.x - bh.x), tf32_rn(bk.y - bh.y), tf32_rn(bk.z - bh.z),
+                        tf32_rn(bk.w - bh.w));
+  }
+}
+
+// Split pass, V: the transposed split V^T [B, H, d, Np] through 32 x 32 tiles
+// in shared memory, so reads (along d) and writes (along n) are both
+// contiguous.  Block (n-tile, c-tile, b * H + h) with 32 x 8 threads; columns
+// n in [N, Np) are written as zeros.
+__global__ void __launch_bounds__(256) split_vt_kernel(const float* v, float* vth, float* vtl,
+                                                       int N, int H, int d, int Np) {
+  __shared__ float tile[32][33];
+  const int n0 = blockIdx.x * 32, c0 = blockIdx.y * 32, bh = blockIdx.z;
+  const int b = bh / H, h = bh % H;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int r = ty; r < 32; r += 8) {
+    const int n = n0 + r, c = c0 + tx;
+    tile[r][tx] = (n < N && c < d) ? v[((static_cast<size_t>(b) * N + n) * H + h) * d + c] : 0.0f;
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int c = c0 + r, n = n0 + tx;
+    if (c < d && n < Np) {
+      const float x = tile[tx][r];
+      const float xh = tf32_rn(x);
+      const size_t o = (static_cast<size_t>(bh) * d + c) * Np + n;
+      vth[o] = xh;
+      vtl[o] = tf32_rn(x - xh);
     }
-    const size_t e = ((static_cast<size_t>(b) * N + n) * H + h) * d + c;
-    const float a = q[e], bk = k[e], bv = v[e];
-    const float ah = tf32_rn(a), bh = tf32_rn(bk), vh = tf32_rn(bv);
-    qh[e] = ah;
-    ql[e] = tf32_rn(a - ah);
-    kh[e] = bh;
-    kl[e] = tf32_rn(bk - bh);
-    vth[vt] = vh;
-    vtl[vt] = tf32_rn(bv - vh);
   }
 }
 
@@ -502,11 +514,19 @@ cudaError_t launch_fwd_tf32x3(const FwdParams& p, void* workspace, cudaStream_t 
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return cudaErrorInvalidDevice;
-  const size_t total = static_cast<size_t>(B) * Np * H * d;
-  const size_t want = (total + 255) / 256, cap = static_cast<size_t>(sms) * 8;
-  split_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
-      static_cast<const float*>(p.q), static_cast<const float*>(p.k),
-      static_cast<const float*>(p.v), qh, ql, kh, kl, vth, vtl, B, N, H, d, Np);
+  // Q and K: B N H d is a multiple of 4 (d is a multiple of 8) and the inputs
+  // are 16-byte aligned.
+  const size_t n4 = static_cast<size_t>(B) * N * H * d / 4;
+  const size_t want = (n4 + 255) / 256, cap = static_cast<size_t>(sms) * 8;
+  split_qk_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
+      static_cast<const float4*>(p.q), static_cast<const float4*>(p.k),
+      reinterpret_cast<float4*>(qh), reinterpret_cast<float4*>(ql), reinterpret_cast<float4*>(kh),
+      reinterpret_cast<float4*>(kl), n4);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (static_cast<long long>(B) * H > 65535) return cudaErrorInvalidConfiguration;
+  split_vt_kernel<<<dim3((Np + 31) / 32, (d + 31) / 32, B * H), 256, 0, st>>>(
+      static_cast<const float*>(p.v), vth, vtl, N, H, d, Np);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ctas = static_cast<long long>(B) * H * ((N + kBM - 1) / kBM);
