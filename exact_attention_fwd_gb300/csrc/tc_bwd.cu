@@ -450,12 +450,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_sp = [&](int cb, int col, int rb) {
       const uint64_t so = static_cast<uint64_t>(((cb % S) * Cfg::kStageBytes) >> 4);
       const uint64_t rbo = static_cast<uint64_t>((rb * Cfg::kRBufBytes) >> 4);
+      auto step = [&](int kk) {
+        const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * Cfg::kRowChunk + (kk & 3) * 32) >> 4);
+        const uint64_t co = static_cast<uint64_t>(((kk >> 2) * Cfg::kBlkChunk + (kk & 3) * 32) >> 4);
+        mma_ss(tmem + Cfg::kTS + col, dR1 + rbo + ro, dC1 + so + co, kIdescSP, kk > 0);
+        mma_ss(tmem + Cfg::kTdP + col, dR2 + rbo + ro, dC2 + so + co, kIdescSP, kk > 0);
+      };
       if (leader) {
-        for (int kk = 0; kk < nks; ++kk) {
-          const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * Cfg::kRowChunk + (kk & 3) * 32) >> 4);
-          const uint64_t co = static_cast<uint64_t>(((kk >> 2) * Cfg::kBlkChunk + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + Cfg::kTS + col, dR1 + rbo + ro, dC1 + so + co, kIdescSP, kk > 0);
-          mma_ss(tmem + Cfg::kTdP + col, dR2 + rbo + ro, dC2 + so + co, kIdescSP, kk > 0);
+        // d = DP in the three-issuer kernel: fully unrolled with constant
+        // offsets (short issue stream); elsewhere the unrolled form costs
+        // spills in the issuing warp, so the loop stays
+        if (kThree && nks == DP / 16) {
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) step(kk);
+        } else {
+          for (int kk = 0; kk < nks; ++kk) step(kk);
         }
       }
       __syncwarp();

@@ -401,8 +401,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t qa = dQ + ((qi * Cfg::kTileBytes) >> 4);
         const uint64_t ka = dK + ((s * Cfg::kTileBytes) >> 4);
         if (leader) {
-          for (int kk = 0; kk < nks; ++kk)
-            mma_ss(tmem + g * kBN, qa + kstep(kk), ka + kstep(kk), kIdescQK, kk > 0);
+          // d = DP = 64: fully unrolled, constant offsets, so the single
+          // issuing thread spends few instructions per MMA (at DP = 128 the
+          // unrolled form costs spills, so the loop stays)
+          if (DP == 64 && nks == DP / 16) {
+#pragma unroll
+            for (int kk = 0; kk < DP / 16; ++kk)
+              mma_ss(tmem + g * kBN, qa + kstep(kk), ka + kstep(kk), kIdescQK, kk > 0);
+          } else {
+            for (int kk = 0; kk < nks; ++kk)
+              mma_ss(tmem + g * kBN, qa + kstep(kk), ka + kstep(kk), kIdescQK, kk > 0);
+          }
           mma_commit(&bars->s_full[g]);
         }
         __syncwarp();

@@ -17,9 +17,11 @@
 //      accesses) and V^T split as [B, H, d, Np] (Np = N rounded up to 4, zeros
 //      beyond N; transposed through shared-memory tiles), so that every MMA
 //      operand is K-major;
-//   2. fused pass, one CTA per (b, h, 128-row Q tile), 6 warps:
-//        warp 0 lane 0   TMA: Qh, Ql once; Kh, Kl, V^Th, V^Tl of each 64-key
-//                        block into a 2-stage ring;
+//   2. fused pass, one CTA per (b, h, 128-row Q tile), 7 warps:
+//        warp 0 lane 0   TMA: Qh, Ql once; Kh, Kl of each 64-key block into a
+//                        3-slot ring that S frees;
+//        warp 6 lane 0   TMA: V^Th, V^Tl of each block into a 2-slot ring that
+//                        P V frees (the K loads run ahead of the V releases);
 //        warp 1 lane 0   MMAs: S = Qh Kh^T + Qh Kl^T + Ql Kh^T (fp32 in TMEM),
 //                        O += Ph Vh + Ph Vl + Pl Vh (P read from TMEM);
 //        warps 2-5       one thread per query row (TMEM lane): masked row max,
@@ -45,16 +47,18 @@ namespace {
 constexpr int kBM = 128;                  // query rows per CTA
 constexpr int kBN = 64;                   // keys per block
 constexpr int kDP = 64;                   // padded head dim (d <= 64)
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
+constexpr int kThreads = 224;
+constexpr int kKStages = 3;               // ring of (Kh, Kl), freed when S has read it
+constexpr int kVStages = 2;               // ring of (Vh, Vl), freed when P V has read it
 constexpr int kQChunk = kBM * 128;        // 32 fp32 columns of 128 rows
 constexpr int kKChunk = kBN * 128;        // 32 fp32 columns of 64 rows
 constexpr int kQTile = 2 * kQChunk;       // 128 x 64 fp32
 constexpr int kKTile = 2 * kKChunk;       // 64 x 64 fp32
 constexpr int kOffQh = 0, kOffQl = kQTile;
-constexpr int kOffStage = 2 * kQTile;     // stage s: Kh, Kl, Vh, Vl
-constexpr int kStageBytes = 4 * kKTile;
-constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+constexpr int kPairBytes = 2 * kKTile;     // one ring slot: hi tile, then lo tile
+constexpr int kOffK = 2 * kQTile;
+constexpr int kOffV = kOffK + kKStages * kPairBytes;
+constexpr int kOffBar = kOffV + kVStages * kPairBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 constexpr int kTmemCols = 256;
@@ -158,8 +162,10 @@ __global__ void __launch_bounds__(256) split_vt_kernel(const float* v, float* vt
 
 struct Tf32Bars {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t s_full, s_free, p_full, pv_done, drain, probe;
   uint32_t tmem_base;
   int abort;
@@ -199,9 +205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, kBM);
@@ -230,43 +240,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   uint8_t* sQh = smem + kOffQh;
   uint8_t* sQl = smem + kOffQl;
-  auto stage = [&](int s) { return smem + kOffStage + s * kStageBytes; };
+  auto kslot = [&](int s) { return smem + kOffK + s * kPairBytes; };
+  auto vslot = [&](int s) { return smem + kOffV + s * kPairBytes; };
 
-  if (run && warp == 0) {
-    // ======================= TMA producer =======================
+  if (run && (warp == 0 || warp == 6)) {
+    // ============ TMA producers: warp 0 loads Q and K, warp 6 loads V ============
+    // (separate rings, so a K load never waits behind the release of a V slot)
     if (lane == 0) {
+      const bool is_k = warp == 0;
+      const int depth = is_k ? kKStages : kVStages;
+      uint64_t* full = is_k ? bars->k_full : bars->v_full;
+      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
       bool ok = true;
-      mbar_arrive_expect_tx(&bars->q_full, 2 * kQTile);
-      for (int ch = 0; ch < 2; ++ch) {
-        tma_load_4d(sQh + ch * kQChunk, &tmQh, &bars->q_full, ch * 32, h, qt * kBM, b);
-        tma_load_4d(sQl + ch * kQChunk, &tmQl, &bars->q_full, ch * 32, h, qt * kBM, b);
+      if (is_k) {
+        mbar_arrive_expect_tx(&bars->q_full, 2 * kQTile);
+        for (int ch = 0; ch < 2; ++ch) {
+          tma_load_4d(sQh + ch * kQChunk, &tmQh, &bars->q_full, ch * 32, h, qt * kBM, b);
+          tma_load_4d(sQl + ch * kQChunk, &tmQl, &bars->q_full, ch * 32, h, qt * kBM, b);
+        }
       }
       int j = 0;
       for (; j < nb; ++j) {
-        const int s = j % kStages, round = j / kStages;
-        if (round > 0 &&
-            !mbar_wait(&bars->kv_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
+        const int s = j % depth, round = j / depth;
+        if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
           ok = false;
           break;
         }
-        uint8_t* st = stage(s);
-        mbar_arrive_expect_tx(&bars->kv_full[s], kStageBytes);
+        uint8_t* slot = is_k ? kslot(s) : vslot(s);
+        mbar_arrive_expect_tx(&full[s], kPairBytes);
         for (int ch = 0; ch < 2; ++ch) {
-          tma_load_4d(st + 0 * kKTile + ch * kKChunk, &tmKh, &bars->kv_full[s], ch * 32, h,
-                      j * kBN, b);
-          tma_load_4d(st + 1 * kKTile + ch * kKChunk, &tmKl, &bars->kv_full[s], ch * 32, h,
-                      j * kBN, b);
-          tma_load_4d(st + 2 * kKTile + ch * kKChunk, &tmVh, &bars->kv_full[s],
-                      j * kBN + ch * 32, 0, h, b);
-          tma_load_4d(st + 3 * kKTile + ch * kKChunk, &tmVl, &bars->kv_full[s],
-                      j * kBN + ch * 32, 0, h, b);
+          if (is_k) {
+            tma_load_4d(slot + ch * kKChunk, &tmKh, &full[s], ch * 32, h, j * kBN, b);
+            tma_load_4d(slot + kKTile + ch * kKChunk, &tmKl, &full[s], ch * 32, h, j * kBN, b);
+          } else {
+            tma_load_4d(slot + ch * kKChunk, &tmVh, &full[s], j * kBN + ch * 32, 0, h, b);
+            tma_load_4d(slot + kKTile + ch * kKChunk, &tmVl, &full[s], j * kBN + ch * 32, 0, h, b);
+          }
         }
       }
       if (!ok) tf32_abort(bars, p.status);
       // every issued copy has landed before the CTA may exit
-      mbar_wait(&bars->q_full, 0, nullptr, kDrainBudget);
-      for (int x = max(0, j - kStages); x < j; ++x)
-        mbar_wait(&bars->kv_full[x % kStages], (x / kStages) & 1, nullptr, kDrainBudget);
+      if (is_k) mbar_wait(&bars->q_full, 0, nullptr, kDrainBudget);
+      for (int x = max(0, j - depth); x < j; ++x)
+        mbar_wait(&full[x % depth], (x / depth) & 1, nullptr, kDrainBudget);
     }
     __syncwarp();
   }
@@ -274,35 +290,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================ MMA issuer (whole warp waits, lane 0 issues) ================
     const bool leader = lane == 0;
     constexpr uint32_t kIdesc = idesc_tf32(kBM, kBN);   // S: N = 64 keys; PV: N = 64 columns
-    const int nks = p.d / 8;                            // K-steps over the head dim
+    // K-steps over the padded head dim: columns >= d of Q and K are zero-filled
+    // by the tensor maps, so a compile-time count (fully unrolled, constant
+    // descriptor offsets) is exact for every d <= 64 and keeps the issuing
+    // thread's instruction stream short.
+    constexpr int nks = kDP / 8;
     const uint64_t dQh = sdesc_sw128(smem_u32(sQh), 16, 1024);
     const uint64_t dQl = sdesc_sw128(smem_u32(sQl), 16, 1024);
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, kWaitBudget));
     auto pv_step = [&](int jj) -> bool {   // O += Ph Vh + Ph Vl + Pl Vh of block jj
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_full, jj & 1, abort_flag, kWaitBudget)))
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&bars->p_full, jj & 1, abort_flag, kWaitBudget) &&
+                          mbar_wait(&bars->v_full[jj % kVStages], (jj / kVStages) & 1, abort_flag,
+                                    kWaitBudget)))
         return false;
       tc_fence_after();
       if (leader) {
-        uint8_t* st = stage(jj % kStages);
-        const uint64_t dVh = sdesc_sw128(smem_u32(st + 2 * kKTile), 16, 1024);
-        const uint64_t dVl = sdesc_sw128(smem_u32(st + 3 * kKTile), 16, 1024);
+        uint8_t* vs = vslot(jj % kVStages);
+        const uint64_t dVh = sdesc_sw128(smem_u32(vs), 16, 1024);
+        const uint64_t dVl = sdesc_sw128(smem_u32(vs + kKTile), 16, 1024);
+#pragma unroll
         for (int kk = 0; kk < kBN / 8; ++kk)
           mma_ts_tf32(tmem + kColO, tmem + kColPh + kk * 8, dVh + kstep(kk, kKChunk), kIdesc,
                       (jj > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
         for (int kk = 0; kk < kBN / 8; ++kk)
           mma_ts_tf32(tmem + kColO, tmem + kColPh + kk * 8, dVl + kstep(kk, kKChunk), kIdesc, 1u);
+#pragma unroll
         for (int kk = 0; kk < kBN / 8; ++kk)
           mma_ts_tf32(tmem + kColO, tmem + kColPl + kk * 8, dVh + kstep(kk, kKChunk), kIdesc, 1u);
         mma_commit(&bars->pv_done);
-        mma_commit(&bars->kv_empty[jj % kStages]);   // S and PV of jj both read the stage
+        mma_commit(&bars->v_empty[jj % kVStages]);
       }
       __syncwarp();
       return true;
     };
     for (int j = 0; j < nb && ok; ++j) {
-      const int s = j % kStages;
+      const int s = j % kKStages;
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(&bars->kv_full[s], (j / kStages) & 1, abort_flag, kWaitBudget) &&
+                      mbar_wait(&bars->k_full[s], (j / kKStages) & 1, abort_flag, kWaitBudget) &&
                           (j == 0 ||
                            mbar_wait(&bars->s_free, (j - 1) & 1, abort_flag, kWaitBudget)))) {
         ok = false;
@@ -310,17 +336,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       if (leader) {
-        uint8_t* st = stage(s);
-        const uint64_t dKh = sdesc_sw128(smem_u32(st), 16, 1024);
-        const uint64_t dKl = sdesc_sw128(smem_u32(st + kKTile), 16, 1024);
+        uint8_t* ks = kslot(s);
+        const uint64_t dKh = sdesc_sw128(smem_u32(ks), 16, 1024);
+        const uint64_t dKl = sdesc_sw128(smem_u32(ks + kKTile), 16, 1024);
+#pragma unroll
         for (int kk = 0; kk < nks; ++kk)
           mma_ss_tf32(tmem + kColS, dQh + kstep(kk, kQChunk), dKh + kstep(kk, kKChunk), kIdesc,
                       kk > 0 ? 1u : 0u);
+#pragma unroll
         for (int kk = 0; kk < nks; ++kk)
           mma_ss_tf32(tmem + kColS, dQh + kstep(kk, kQChunk), dKl + kstep(kk, kKChunk), kIdesc, 1u);
+#pragma unroll
         for (int kk = 0; kk < nks; ++kk)
           mma_ss_tf32(tmem + kColS, dQl + kstep(kk, kQChunk), dKh + kstep(kk, kKChunk), kIdesc, 1u);
         mma_commit(&bars->s_full);
+        mma_commit(&bars->k_empty[s]);
       }
       __syncwarp();
       if (j > 0 && !pv_step(j - 1)) ok = false;
@@ -331,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit_w(&bars->drain, leader ? 1u : 0u);
     mbar_wait(&bars->drain, 0, nullptr, kDrainBudget);
     __syncwarp();
-  } else if (run && warp >= 2) {
+  } else if (run && warp >= 2 && warp <= 5) {
     // ======================= softmax / epilogue (warps 2-5) =======================
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
