@@ -464,7 +464,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) step(kk);
         } else {
-          for (int kk = 0; kk < nks; ++kk) step(kk);
+          // descriptors advanced in place: +32 B per K=16 step inside a
+          // 64-column chunk, then on to the next chunk
+          uint64_t a1 = dR1 + rbo, a2 = dR2 + rbo, b1 = dC1 + so, b2 = dC2 + so;
+          constexpr uint64_t kRowJump = (Cfg::kRowChunk - 96) >> 4;
+          constexpr uint64_t kBlkJump = (Cfg::kBlkChunk - 96) >> 4;
+          for (int kk = 0; kk < nks; ++kk) {
+            mma_ss(tmem + Cfg::kTS + col, a1, b1, kIdescSP, kk > 0);
+            mma_ss(tmem + Cfg::kTdP + col, a2, b2, kIdescSP, kk > 0);
+            const bool wrap = (kk & 3) == 3;
+            a1 += wrap ? kRowJump : 2;
+            a2 += wrap ? kRowJump : 2;
+            b1 += wrap ? kBlkJump : 2;
+            b2 += wrap ? kBlkJump : 2;
+          }
         }
       }
       __syncwarp();

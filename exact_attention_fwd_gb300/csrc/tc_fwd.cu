@@ -409,8 +409,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < DP / 16; ++kk)
               mma_ss(tmem + g * kBN, qa + kstep(kk), ka + kstep(kk), kIdescQK, kk > 0);
           } else {
-            for (int kk = 0; kk < nks; ++kk)
-              mma_ss(tmem + g * kBN, qa + kstep(kk), ka + kstep(kk), kIdescQK, kk > 0);
+            // descriptors advanced in place: +32 B per K=16 step inside a
+            // 64-column chunk, then on to the next chunk
+            constexpr uint64_t kJump = (kChunkBytes - 96) >> 4;
+            uint64_t a = qa, b = ka;
+            for (int kk = 0; kk < nks; ++kk) {
+              mma_ss(tmem + g * kBN, a, b, kIdescQK, kk > 0);
+              const uint64_t inc = (kk & 3) == 3 ? kJump : 2;
+              a += inc;
+              b += inc;
+            }
           }
           mma_commit(&bars->s_full[g]);
         }
