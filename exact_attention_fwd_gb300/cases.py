@@ -16,7 +16,12 @@ forward):
 * ``tf32x3``: B8 H16 N1024 d64 causal float32, ``forward_tf32x3`` (split pass
   plus one tensor-core kernel);
 * ``splitkv``: B1 H1 N32768 d128 causal bf16, ``forward_splitkv`` with 8 key
-  slices (partial forward plus merge).
+  slices (partial forward plus merge);
+* ``bert_fwd`` / ``bert_bwd``: B64 H16 N512 d64 non-causal bf16, Q and K with
+  standard deviation 4, ``forward`` / ``backward`` (backward FLOP 2.5 times the
+  forward's);
+* ``long4_fwd`` / ``long4_bwd``: B4 H32 N8192 d128 causal bf16, ``forward`` /
+  ``backward``.
 """
 import argparse
 
@@ -80,11 +85,31 @@ def _case_splitkv(dev):
         lambda: api.forward_splitkv(q, k, v, S, causal=True, out=o, lse=lse, ws=ws)
 
 
+def _fwd_bwd_pair(B, H, N, d, causal, qk_std, dev, backward):
+    q, k, v, do = _inputs((B, N, H, d), torch.float32, dev, count=4)
+    q, k = (t * qk_std for t in (q, k))
+    q, k, v, do = (t.to(torch.bfloat16) for t in (q, k, v, do))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device=dev)
+    flop = 4.0 * B * H * d * _pairs(N, causal)
+    if not backward:
+        return (B, H, N, d), flop, lambda: api.forward(q, k, v, causal=causal, out=o, lse=lse)
+    api.forward(q, k, v, causal=causal, out=o, lse=lse)
+    ws = api.workspace(B, H, N, dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    return (B, H, N, d), 2.5 * flop, lambda: api.backward(
+        q, k, v, o, lse, do, causal=causal, ws=ws, dq=dq, dk=dk, dv=dv)
+
+
 CASES = {
     "long_fwd": _case_long_fwd,
     "gpt2_unfused": _case_gpt2_unfused,
     "tf32x3": _case_tf32x3,
     "splitkv": _case_splitkv,
+    "bert_fwd": lambda dev: _fwd_bwd_pair(64, 16, 512, 64, False, 4.0, dev, False),
+    "bert_bwd": lambda dev: _fwd_bwd_pair(64, 16, 512, 64, False, 4.0, dev, True),
+    "long4_fwd": lambda dev: _fwd_bwd_pair(4, 32, 8192, 128, True, 1.0, dev, False),
+    "long4_bwd": lambda dev: _fwd_bwd_pair(4, 32, 8192, 128, True, 1.0, dev, True),
 }
 
 

@@ -10,7 +10,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_case_registry_matches_documented_names():
-    assert sorted(cases.CASES) == ["gpt2_unfused", "long_fwd", "splitkv", "tf32x3"]
+    assert sorted(cases.CASES) == ["bert_bwd", "bert_fwd", "gpt2_unfused", "long4_bwd",
+                                   "long4_fwd", "long_fwd", "splitkv", "tf32x3"]
     doc = cases.__doc__
     for name in cases.CASES:
         assert f"``{name}``" in doc
