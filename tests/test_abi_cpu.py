@@ -243,3 +243,16 @@ def test_tf32x3_rejects_invalid_arguments(lib, kw, want):
              scale=0.125, causal=1, workspace=16 * FAKE, workspace_bytes=1 << 22, stream=None)
     a.update(kw)
     assert _lib.fa_fwd_tf32x3(**a) == want
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    """No fallback: without libfa.so every binding raises instead of computing."""
+    from exact_attention_fwd_gb300 import _lib
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libfa.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    for call in (lambda: _lib.load(),
+                 lambda: _lib.fa_bwd_workspace_size(1, 1, 128),
+                 lambda: _lib.fa_fwd_tf32x3_workspace_size(1, 1, 128, 64),
+                 lambda: _lib.fa_fwd_unfused_workspace_size(1, 1, 128, 64)):
+        with pytest.raises(RuntimeError, match="not built"):
+            call()
