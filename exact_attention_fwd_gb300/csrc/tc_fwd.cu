@@ -135,8 +135,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, budget));
 }
 
-// Work item -> (b, h) and its two adjacent Q tiles (2p, 2p+1); tile[0] is the
-// later, longer one under the causal mask.  The two tiles' softmax
+// Work item -> (b, h) and its two adjacent Q tiles (2p, 2p+1); with one tile
+// (odd tile count, last pair) it is tile[0].  The two tiles' softmax
 // warpgroups are both busy for all but the last block, so their MMAs and
 // exponentials interleave.
 struct Item {
@@ -204,6 +204,13 @@ __device__ __forceinline__ Item decode_item(int it, int nq, int nk, int H, int s
   const int lo = 2 * pr, hi = 2 * pr + 1;
   r.tile[0] = (hi < nq) ? hi : lo;
   r.tile[1] = (hi < nq) ? lo : -1;
+  // Causal: the later tile reads one block more.  Odd items give it to slot
+  // 1, so neither slot's lead over the other grows from item to item (the
+  // shared K/V ring caps that lead, and a slot at the cap would idle).
+  if (kCausal && (it & 1) && r.tile[1] >= 0) {
+    r.tile[0] = lo;
+    r.tile[1] = hi;
+  }
 #pragma unroll
   for (int g = 0; g < kQT; ++g) {
     const int all = (r.tile[g] < 0) ? 0 : (kCausal ? min(nk, r.tile[g] + 1) : nk);
@@ -340,6 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ch = 0; ch < Cfg::kChunks; ++ch)
             tma_load_4d(sV + s * Cfg::kTileBytes + ch * kChunkBytes, &tmV, &bars->v_full[s],
                         ch * 64, w.h, (w.j0 + j) * kBN, w.b);
+          // Separate-P layout: a tile slot that does not read this block
+          // (the shorter causal tile's last block, an absent tile) has its
+          // release made here: the stage's previous round is complete, so
+          // the arrival counts toward this one.
+          if constexpr (Cfg::kSepP)
+            for (int g = 0; g < kQT; ++g)
+              if (j >= w.nblk[g]) mbar_arrive(&bars->kv_empty[s]);
           ++c;
         }
       }
@@ -451,15 +465,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One MMA warp per Q tile slot (g = warp - 1), so the two tiles never
         // wait on each other's softmax.  Per block j of the tile: S(j) as soon
         // as the softmax has S(j-1) in registers, then O += P(j-1) V(j-1) as
-        // soon as P(j-1) is in TMEM.  One commit per MMA group (each costs
-        // tensor-pipe time): s_full after S, pv_done after PV; the softmax
-        // warpgroup releases K/V stages once it has seen the PV complete.
+        // soon as P(j-1) is in TMEM.  The sequence runs on across items: the
+        // next item's S(0) is issued before this item's last P V (the softmax
+        // writes the finished item's O out between its next item's first
+        // block and that block's P, so the next P V finds O read).  One
+        // commit per MMA group (each costs tensor-pipe time): s_full after S,
+        // pv_done after P V; the softmax warpgroup releases K/V stages once
+        // it has seen the P V complete.
         const int g = warp - 1;
-        int qn = 0;
+        int qn = 0;     // Q buffers consumed
+        // the P V still to issue: its K/V block index and accumulate flag
+        bool pend = false, pend_acc = false, pend_last = false;
+        int pend_x = 0;
+        auto issue_pending = [&]() -> bool {   // O += P V of the pending block
+          const int s = pend_x % S;
+          if (!warp_wait(&bars->v_full[s], (pend_x / S) & 1, abort_flag, kWaitBudget) ||
+              !warp_wait(&bars->p_full[g], pc[g] & 1, abort_flag, kWaitBudget))
+            return false;
+          ++pc[g];
+          tc_fence_after();
+          issue_pv(g, s, pend_acc);
+          mma_commit_w(&bars->pv_done[g], leader);
+          // an item's last block: this slot's release of its stage, made
+          // when the P V has read it (the softmax releases the others)
+          if (pend_last) mma_commit_w(&bars->kv_empty[s], leader);
+          pend = false;
+          return true;
+        };
         for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
           const Item w = decode_item<kCausal, kSplit>(it, nq, nk, H, p.split_blocks);
           const int nb = w.nblk[g];
           const int qb = qn & 1;   // Q buffer of this item (its load number is qn)
+          // The pending P V is the previous item's last.  The softmax's
+          // release of that item's last stages waits for it, and the
+          // producer may need those releases before this item's first K/V
+          // block can land; so it is issued first unless that block is
+          // already there (then S(0) goes ahead of it without waiting).
+          if (pend && (nb == 0 || !__all_sync(0xffffffffu,
+                                             mbar_try_wait(&bars->k_full[c % S], (c / S) & 1))) &&
+              !issue_pending()) {
+            ok = false;
+            break;
+          }
           if (nb > 0) {
             if (!warp_wait(&bars->q_full[g][qb], (qn >> 1) & 1, abort_flag, kWaitBudget)) {
               ok = false;
@@ -467,17 +514,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++qn;
           }
-          auto pv_step = [&](int j) -> bool {   // O += P(j) V(j)
-            const int cj = c + j, s = cj % S;
-            if (!warp_wait(&bars->v_full[s], (cj / S) & 1, abort_flag, kWaitBudget) ||
-                !warp_wait(&bars->p_full[g], pc[g] & 1, abort_flag, kWaitBudget))
-              return false;
-            ++pc[g];
-            tc_fence_after();
-            issue_pv(g, s, j > 0);
-            mma_commit_w(&bars->pv_done[g], leader);
-            return true;
-          };
           for (int j = 0; j < nb && ok; ++j) {
             const int cj = c + j, s = cj % S;
             if (!warp_wait(&bars->k_full[s], (cj / S) & 1, abort_flag, kWaitBudget) ||
@@ -492,12 +528,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the tile's last scores are issued: once they complete, the
             // producer may reload this Q buffer
             if (j == nb - 1) mma_commit_w(&bars->q_empty[g][qb], leader);
-            if (j > 0 && !pv_step(j - 1)) ok = false;
+            if (pend && !issue_pending()) {
+              ok = false;
+              break;
+            }
+            pend = true;
+            pend_x = cj;
+            pend_acc = j > 0;
+            pend_last = j == nb - 1;
           }
-          if (ok && nb > 0 && !pv_step(nb - 1)) ok = false;
           if (!ok) break;
           c += w.nmax;
         }
+        if (ok && pend && !issue_pending()) ok = false;
       } else {
         for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
           const Item w = decode_item<kCausal, kSplit>(it, nq, nk, H, p.split_blocks);
@@ -578,27 +621,162 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kc = 0;    // K/V blocks of the items before this one (separate-P layout)
     bool ok = true;
     // Separate-P layout: this warpgroup's release of the K/V stage of global
-    // block x, once its own MMAs no longer read it.  For a block the tile does
-    // not visit, the release waits until the block has landed, so it counts
-    // toward that round of the stage and never toward the previous one.
-    auto release_kv = [&](int x, bool wait_landed) -> bool {
-      if (wait_landed &&
-          !__all_sync(0xffffffffu, mbar_wait(&bars->k_full[x % S], (x / S) & 1, abort_flag,
-                                             kWaitBudget)))
-        return false;
+    // block x, once its own MMAs no longer read it (every block the tile
+    // reads but its item's last; the MMA warp releases that one, the
+    // producer the blocks the tile skips).
+    auto release_kv = [&](int x) {
       if (row == 0) mbar_arrive(&bars->kv_empty[x % S]);
-      return true;
     };
 
+    // Write an item's output rows: O / l rounded once to 16 bits (split-KV:
+    // float32 O over the slice), L = (m + log2 l) ln 2.  Called once the
+    // item's last O += P V has completed.
+    auto write_out = [&](const Item& ew, int eqt, float em, float el) -> bool {
+      const int eq_row = eqt * kBM + row;
+      tc_fence_after();
+      const bool live = el > 0.0f;
+      const float inv = live ? 1.0f / el : 0.0f;
+      const bool store = eq_row < N;
+      if constexpr (kSplit) {
+        // split-KV partial: O normalised over the slice, float32, straight
+        // from registers (one 16-byte store per 4 columns of the row)
+        float* orow = p.o_part +
+                      ((static_cast<size_t>(ew.split) * p.B + ew.b) * N + (store ? eq_row : 0)) *
+                          static_cast<size_t>(H) * p.d +
+                      static_cast<size_t>(ew.h) * p.d;
+#pragma unroll
+        for (int cc = 0; cc < DP / 32; ++cc) {
+          uint32_t orr[32];
+          __syncwarp();   // the stores below are per-thread; tcgen05.ld is collective
+          tmem_ld32(tO + cc * 32, orr);
+          tmem_ld_wait(orr);
+          if (store) {
+#pragma unroll
+            for (int qv = 0; qv < 8; ++qv) {
+              const int col = cc * 32 + qv * 4;
+              if (col < p.d)
+                *reinterpret_cast<float4*>(orow + col) =
+                    make_float4(__uint_as_float(orr[qv * 4 + 0]) * inv,
+                                __uint_as_float(orr[qv * 4 + 1]) * inv,
+                                __uint_as_float(orr[qv * 4 + 2]) * inv,
+                                __uint_as_float(orr[qv * 4 + 3]) * inv);
+            }
+          }
+        }
+      } else if constexpr (Cfg::kSepP) {
+        // Stage the bf16 O tile in shared memory in the TMA box layout (rows
+        // of 128 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7)), then
+        // one thread stores it with a TMA tensor store (rows >= N and columns
+        // >= d are not written).  The staging tile is reused once the previous
+        // store has read it.
+        // (mbarrier handshakes, so that every wait is bounded)
+        uint8_t* stage = sO + g * Cfg::kTileBytes;
+        const int e = oc - 1;   // epilogues of this slot so far
+        if (row == 0) {
+          bulk_wait_read_all();
+          mbar_arrive(&bars->stage_free[g]);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->stage_free[g], e & 1, abort_flag,
+                                               kWaitBudget))) {
+          ok = false;
+          return false;
+        }
+#pragma unroll
+        for (int cc = 0; cc < DP / 32; ++cc) {
+          uint32_t orr[32];
+          __syncwarp();   // tcgen05.ld is warp-collective
+          tmem_ld32(tO + cc * 32, orr);
+          tmem_ld_wait(orr);
+#pragma unroll
+          for (int qv = 0; qv < 4; ++qv) {
+            const int chunk = cc * 4 + qv;   // 16-byte chunk of the row (8 columns)
+            uint4 v;
+            v.x = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 0]) * inv,
+                              __uint_as_float(orr[qv * 8 + 1]) * inv);
+            v.y = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 2]) * inv,
+                              __uint_as_float(orr[qv * 8 + 3]) * inv);
+            v.z = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 4]) * inv,
+                              __uint_as_float(orr[qv * 8 + 5]) * inv);
+            v.w = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 6]) * inv,
+                              __uint_as_float(orr[qv * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4)) = v;
+          }
+        }
+        fence_proxy_async_smem();   // the TMA engine reads what the threads wrote
+        mbar_arrive(&bars->stage_full[g]);
+        if (row == 0) {
+          if (!mbar_wait(&bars->stage_full[g], e & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+          } else {
+            tma_store_4d(&tmO, stage, 0, ew.h, eqt * kBM, ew.b);
+            bulk_commit_group();
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          return false;
+        }
+      } else {
+        __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
+        uint4* orow = reinterpret_cast<uint4*>(
+            O + ((static_cast<size_t>(ew.b) * N + (store ? eq_row : 0)) * H + ew.h) * p.d);
+#pragma unroll
+        for (int cc = 0; cc < DP / 32; ++cc) {
+          uint32_t orr[32];
+          __syncwarp();   // the stores below are per-thread; tcgen05.ld is collective
+          tmem_ld32(tO + cc * 32, orr);
+          tmem_ld_wait(orr);
+          if (store) {
+#pragma unroll
+            for (int qv = 0; qv < 4; ++qv) {
+              const int col = cc * 32 + qv * 8;
+              if (col < p.d) {
+                uint4 v;
+                v.x = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 0]) * inv,
+                                  __uint_as_float(orr[qv * 8 + 1]) * inv);
+                v.y = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 2]) * inv,
+                                  __uint_as_float(orr[qv * 8 + 3]) * inv);
+                v.z = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 4]) * inv,
+                                  __uint_as_float(orr[qv * 8 + 5]) * inv);
+                v.w = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 6]) * inv,
+                                  __uint_as_float(orr[qv * 8 + 7]) * inv);
+                orow[col / 8] = v;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      if (store) {
+        const float L = live ? (em + __log2f(el)) * 0.69314718055994531f : -INFINITY;
+        if constexpr (kSplit)
+          p.lse_part[((static_cast<size_t>(ew.split) * p.B + ew.b) * H + ew.h) * N + eq_row] = L;
+        else
+          p.lse[(static_cast<size_t>(ew.b) * H + ew.h) * N + eq_row] = L;
+      }
+      return true;
+    };
+    // Separate-P layout: the item whose output is still to be written
+    bool epi_pend = false;
+    Item ew{};
+    int eqt = 0;
+    float em = 0.0f, el = 0.0f;
+    // Write out the pending item, after waiting for its last P V unless the
+    // caller has.
+    auto finish_pending = [&](bool wait_pv) -> bool {
+      if (wait_pv && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[g], (sc - 1) & 1,
+                                                        abort_flag, kWaitBudget)))
+        return false;
+      ++oc;
+      epi_pend = false;
+      return write_out(ew, eqt, em, el);
+    };
     int li = 0;
     for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
       const Item w = decode_item<kCausal, kSplit>(it, nq, nk, H, p.split_blocks);
       const int qt = w.tile[g];
       if (qt < 0) {
-        if constexpr (Cfg::kSepP) {
-          for (int j = 0; j < w.nmax && ok; ++j) ok = release_kv(kc + j, true);
-          kc += w.nmax;
-        }
+        if constexpr (Cfg::kSepP) kc += w.nmax;   // the producer releases its stages
         continue;
       }
       const int q_row = qt * kBM + row;
@@ -716,9 +894,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          // block j-1's MMAs are done (the previous item's last block was
-          // released by that item's epilogue)
-          if (j > 0) release_kv(kc + j - 1, false);
+          // block j-1's MMAs are done (the previous item's last block is
+          // released with its deferred epilogue, here at j = 0)
+          if (j > 0) release_kv(kc + j - 1);
+          if (j == 0 && epi_pend && !finish_pending(false)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           if (rescale) rescale_o();
           __syncwarp();
@@ -735,145 +917,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
 
-      // ---- epilogue: O / l -> bf16, L = (m + log2 l) ln 2 ----
-      // Separate-P layout: the last block's pv_done phase (its PV is the
-      // tile's last MMA); then the item's remaining K/V stages are released.
-      if (!__all_sync(0xffffffffu,
-                      Cfg::kSepP
-                          ? mbar_wait(&bars->pv_done[g], (sc - 1) & 1, abort_flag, kWaitBudget)
-                          : mbar_wait(&bars->o_final[g], oc & 1, abort_flag, kWaitBudget))) {
-        ok = false;
-        break;
-      }
-      ++oc;
       if constexpr (Cfg::kSepP) {
-        release_kv(kc + w.nblk[g] - 1, false);
-        for (int j = w.nblk[g]; j < w.nmax && ok; ++j) ok = release_kv(kc + j, true);
+        // The epilogue is deferred: it runs during the next item's first
+        // block, between that block's exponentials and its P store, by when
+        // this item's last P V has long completed.
+        epi_pend = true;
+        ew = w;
+        eqt = qt;
+        em = m_ref;
+        el = l;
         kc += w.nmax;
-        if (!ok) break;
-      }
-      tc_fence_after();
-      const bool live = l > 0.0f;
-      const float inv = live ? 1.0f / l : 0.0f;
-      const bool store = q_row < N;
-      if constexpr (kSplit) {
-        // split-KV partial: O normalised over the slice, float32, straight
-        // from registers (one 16-byte store per 4 columns of the row)
-        float* orow = p.o_part +
-                      ((static_cast<size_t>(w.split) * p.B + w.b) * N + (store ? q_row : 0)) *
-                          static_cast<size_t>(H) * p.d +
-                      static_cast<size_t>(w.h) * p.d;
-#pragma unroll
-        for (int cc = 0; cc < DP / 32; ++cc) {
-          uint32_t orr[32];
-          __syncwarp();   // the stores below are per-thread; tcgen05.ld is collective
-          tmem_ld32(tO + cc * 32, orr);
-          tmem_ld_wait(orr);
-          if (store) {
-#pragma unroll
-            for (int qv = 0; qv < 8; ++qv) {
-              const int col = cc * 32 + qv * 4;
-              if (col < p.d)
-                *reinterpret_cast<float4*>(orow + col) =
-                    make_float4(__uint_as_float(orr[qv * 4 + 0]) * inv,
-                                __uint_as_float(orr[qv * 4 + 1]) * inv,
-                                __uint_as_float(orr[qv * 4 + 2]) * inv,
-                                __uint_as_float(orr[qv * 4 + 3]) * inv);
-            }
-          }
-        }
-      } else if constexpr (Cfg::kSepP) {
-        // Stage the bf16 O tile in shared memory in the TMA box layout (rows
-        // of 128 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7)), then
-        // one thread stores it with a TMA tensor store (rows >= N and columns
-        // >= d are not written).  The staging tile is reused once the previous
-        // store has read it.
-        // (mbarrier handshakes, so that every wait is bounded)
-        uint8_t* stage = sO + g * Cfg::kTileBytes;
-        const int e = oc - 1;   // epilogues of this slot so far
-        if (row == 0) {
-          bulk_wait_read_all();
-          mbar_arrive(&bars->stage_free[g]);
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->stage_free[g], e & 1, abort_flag,
-                                               kWaitBudget))) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int cc = 0; cc < DP / 32; ++cc) {
-          uint32_t orr[32];
-          __syncwarp();   // tcgen05.ld is warp-collective
-          tmem_ld32(tO + cc * 32, orr);
-          tmem_ld_wait(orr);
-#pragma unroll
-          for (int qv = 0; qv < 4; ++qv) {
-            const int chunk = cc * 4 + qv;   // 16-byte chunk of the row (8 columns)
-            uint4 v;
-            v.x = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 0]) * inv,
-                              __uint_as_float(orr[qv * 8 + 1]) * inv);
-            v.y = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 2]) * inv,
-                              __uint_as_float(orr[qv * 8 + 3]) * inv);
-            v.z = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 4]) * inv,
-                              __uint_as_float(orr[qv * 8 + 5]) * inv);
-            v.w = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 6]) * inv,
-                              __uint_as_float(orr[qv * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4)) = v;
-          }
-        }
-        fence_proxy_async_smem();   // the TMA engine reads what the threads wrote
-        mbar_arrive(&bars->stage_full[g]);
-        if (row == 0) {
-          if (!mbar_wait(&bars->stage_full[g], e & 1, abort_flag, kWaitBudget)) {
-            ok = false;
-          } else {
-            tma_store_4d(&tmO, stage, 0, w.h, qt * kBM, w.b);
-            bulk_commit_group();
-          }
-        }
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
       } else {
-        __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
-        uint4* orow = reinterpret_cast<uint4*>(
-            O + ((static_cast<size_t>(w.b) * N + (store ? q_row : 0)) * H + w.h) * p.d);
-#pragma unroll
-        for (int cc = 0; cc < DP / 32; ++cc) {
-          uint32_t orr[32];
-          __syncwarp();   // the stores below are per-thread; tcgen05.ld is collective
-          tmem_ld32(tO + cc * 32, orr);
-          tmem_ld_wait(orr);
-          if (store) {
-#pragma unroll
-            for (int qv = 0; qv < 4; ++qv) {
-              const int col = cc * 32 + qv * 8;
-              if (col < p.d) {
-                uint4 v;
-                v.x = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 0]) * inv,
-                                  __uint_as_float(orr[qv * 8 + 1]) * inv);
-                v.y = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 2]) * inv,
-                                  __uint_as_float(orr[qv * 8 + 3]) * inv);
-                v.z = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 4]) * inv,
-                                  __uint_as_float(orr[qv * 8 + 5]) * inv);
-                v.w = pack16x2<kF16>(__uint_as_float(orr[qv * 8 + 6]) * inv,
-                                  __uint_as_float(orr[qv * 8 + 7]) * inv);
-                orow[col / 8] = v;
-              }
-            }
-          }
+        // ---- epilogue (aliased layout) ----
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&bars->o_final[g], oc & 1, abort_flag, kWaitBudget))) {
+          ok = false;
+          break;
         }
-      }
-      tc_fence_before();
-      if (store) {
-        const float L = live ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        if constexpr (kSplit)
-          p.lse_part[((static_cast<size_t>(w.split) * p.B + w.b) * H + w.h) * N + q_row] = L;
-        else
-          p.lse[(static_cast<size_t>(w.b) * H + w.h) * N + q_row] = L;
+        ++oc;
+        if (!write_out(w, qt, m_ref, l)) {
+          ok = false;
+          break;
+        }
       }
     }
+    if (ok && epi_pend) ok = finish_pending(true);
     if (!ok) raise_abort(bars, p.status);
     // the O stores must have completed (and read shared memory) before exit
     if (Cfg::kSepP && row == 0) bulk_wait_all();
