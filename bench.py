@@ -204,6 +204,115 @@ def cpu_oracle_rate(inp, scale, causal, budget_s, max_heads=None):
 
 
 # ----------------------------------------------------------------------------
+# the other workloads, timed after the main region
+# ----------------------------------------------------------------------------
+
+def _event_ms(fn, stream, reps, flush=None):
+    """Median over `reps` of fn()'s device time (CUDA events on `stream`);
+    `flush`, when given, runs before each rep outside the events."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def time_other_workloads(dev, peaks, reps_large=10, reps_small=30):
+    """Forward and backward of the BERT-large-shaped and long-context
+    workloads (TFLOP/s and % of the bf16 peak), and the short-N parity
+    shapes (microseconds per call and GB/s of algorithmic bytes, L2 flushed
+    before every call).  Inputs: seeded normals drawn on the device."""
+    import torch
+
+    from exact_attention_fwd_gb300 import api
+    from exact_attention_fwd_gb300.configs import (WORKLOADS, bytes_bwd, bytes_fwd, flops_bwd,
+                                                  flops_fwd)
+    stream = torch.cuda.current_stream(dev)
+    gen = torch.Generator(device=dev)
+    pk = peaks["bf16_tflops"]
+
+    def make(B, H, N, d, dtype, sigma_qk, seed):
+        gen.manual_seed(seed)
+        t = [torch.randn(B, N, H, d, device=dev, generator=gen, dtype=torch.float32)
+             for _ in range(4)]
+        t[0].mul_(sigma_qk)
+        t[1].mul_(sigma_qk)
+        return [x.to(dtype) for x in t]
+
+    def run(B, H, N, d, causal, dtype, sigma_qk, seed, reps, flush=None, backward=True):
+        q, k, v, do = make(B, H, N, d, dtype, sigma_qk, seed)
+        o, lse = torch.empty_like(q), torch.empty(B, H, N, device=dev)
+        ws = api.workspace(B, H, N, dev)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        scale = 1.0 / math.sqrt(d)
+
+        def fwd():
+            api.forward(q, k, v, scale=scale, causal=causal, out=o, lse=lse)
+
+        def bwd():
+            api.backward(q, k, v, o, lse, do, scale=scale, causal=causal, ws=ws, dq=dq, dk=dk,
+                         dv=dv)
+        for _ in range(3):
+            fwd()
+            if backward:
+                bwd()
+        torch.cuda.synchronize(dev)
+        out = {"fwd_ms": _event_ms(fwd, stream, reps, flush)}
+        if backward:
+            out["bwd_ms"] = _event_ms(bwd, stream, reps, flush)
+        if api.sync_status() != 0:
+            raise SystemExit(f"device status word set in workload B{B} H{H} N{N} d{d}")
+        return out
+
+    res = {}
+    for key, w in (("bert_large", WORKLOADS[3]), ("long_context", WORKLOADS[4])):
+        sh = w.shapes[0]
+        t = run(sh.B, sh.H, sh.N, sh.d, w.causal, torch.bfloat16, w.sigma.get("q", 1.0),
+                2100 + w.index, reps_large)
+        ff, fb = flops_fwd(sh.B, sh.H, sh.N, sh.d, w.causal), flops_bwd(sh.B, sh.H, sh.N, sh.d,
+                                                                         w.causal)
+        res[key] = {"workload": w.name, "causal": w.causal, "sigma_qk": w.sigma.get("q", 1.0),
+                    "fwd": {"ms": round(t["fwd_ms"], 4),
+                            "tflops": round(ff / t["fwd_ms"] / 1e9, 1),
+                            "pct_peak": round(100 * ff / t["fwd_ms"] / 1e9 / pk, 2)},
+                    "bwd": {"ms": round(t["bwd_ms"], 4),
+                            "tflops": round(fb / t["bwd_ms"] / 1e9, 1),
+                            "pct_peak": round(100 * fb / t["bwd_ms"] / 1e9 / pk, 2)},
+                    "reps": reps_large}
+    # short-N shapes: latency-bound; L2 flushed (a 256 MB write) before each call
+    junk = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        junk.fill_(1)
+    short = []
+    shapes = [(WORKLOADS[0], sh, dt) for sh in WORKLOADS[0].shapes for dt in WORKLOADS[0].dtypes]
+    shapes += [(WORKLOADS[1], sh, dt) for sh in WORKLOADS[1].shapes for dt in WORKLOADS[1].dtypes]
+    for w, sh, dt in shapes:
+        tdt = torch.float32 if dt == "f32" else torch.bfloat16
+        elt = 4 if dt == "f32" else 2
+        t = run(sh.B, sh.H, sh.N, sh.d, w.causal, tdt, 1.0, 2200 + w.index, reps_small,
+                flush=flush, backward=w.backward)
+        e = {"workload": w.name, "B": sh.B, "H": sh.H, "N": sh.N, "d": sh.d, "dtype": dt,
+             "causal": w.causal, "fwd_us": round(1e3 * t["fwd_ms"], 2),
+             "fwd_gbs": round(bytes_fwd(sh.B, sh.H, sh.N, sh.d, elt) / t["fwd_ms"] / 1e6, 2)}
+        if w.backward:
+            e["bwd_us"] = round(1e3 * t["bwd_ms"], 2)
+            e["bwd_gbs"] = round(bytes_bwd(sh.B, sh.H, sh.N, sh.d, elt) / t["bwd_ms"] / 1e6, 2)
+        short.append(e)
+    res["short_n"] = {"timing": f"median of {reps_small} calls, L2 flushed before each",
+                      "hbm_peak_gbs": peaks["hbm_gbs"], "shapes": short}
+    del junk
+    return res
+
+
+# ----------------------------------------------------------------------------
 # distributed plumbing
 # ----------------------------------------------------------------------------
 
@@ -390,6 +499,10 @@ def run_ours(args, rank, local_rank, world):
                    "max_abs_diff_vs_fused": float((o_u.float() - o.float()).abs().max())}
         del uws
 
+    others = None
+    if rank == 0 and not args.no_other_workloads:
+        others = time_other_workloads(dev, load_peaks()[0])
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, nh, secs = cpu_oracle_rate(inp, scale, causal, args.cpu_seconds)
@@ -426,6 +539,7 @@ def run_ours(args, rank, local_rank, world):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "unfused_fwd": unfused,
+        "other_workloads": others,
         "gpu_launches": 4 * K,
         "clocks": clk.summary(),
     }
@@ -484,6 +598,8 @@ def main(argv=None):
     ap.add_argument("--no-unfused", action="store_true",
                     help="skip timing the unfused comparison forward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip timing the BERT-shaped, long-context and short-N workloads")
     ap.add_argument("--batch", type=int, default=0,
                     help="override B (profiler captures of a smaller case); 0 = the workload's")
     args = ap.parse_args(argv)

@@ -136,6 +136,17 @@ fa_status fa_bwd_phase(int phase, const void* q, const void* k, const void* v, c
  * status word of the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel's
  * bounded wait ran out since the last call (its outputs are then undefined),
  * or FA_ERR_CUDA if the synchronisation itself failed.
+ *
+ * The status word is one int per device, shared by every stream and every
+ * caller on that device (it is not in the caller's workspace).  A timeout
+ * recorded by a kernel on stream A is therefore returned, and cleared, by
+ * whichever fa_sync_status call on that device reads it first, whatever
+ * stream that call names; and since only `stream` is synchronised, a kernel
+ * still running on another stream may record a timeout after the read.
+ * Callers that run library kernels on several streams and need to know
+ * which call timed out should synchronise all of those streams (e.g.
+ * cudaDeviceSynchronize) before calling fa_sync_status, or serialise the
+ * calls they want to tell apart.
  */
 fa_status fa_sync_status(void* stream);
 

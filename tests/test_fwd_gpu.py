@@ -162,3 +162,28 @@ def test_many_items_per_cta(causal, N, d):
     o, lse, _ = run_fwd(inp, causal=causal)
     heads = [(0, 0), (B - 1, H - 1), (17, 5), (23, 11), (39, 0)]
     compare_fwd(inp, o, lse, causal, default_scale(d), heads=heads)
+
+
+def test_status_word_is_shared_across_streams():
+    """The device status word is one per device: a timeout recorded by a
+    kernel on stream A is what fa_sync_status on stream B reports, and that
+    call clears it for A as well (documented in include/fa.h)."""
+    torch = require_gpu()
+    from exact_attention_fwd_gb300 import _lib, api
+    inp = make(1, 2, 256, 64, "bf16", 8801)
+    dev = torch.device("cuda", 0)
+    q, k, v = (inp.torch(t, dev) for t in ("q", "k", "v"))
+    sa, sb = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)
+    assert api.sync_status() == 0
+    os.environ["FA_SELFTEST_WAIT_TIMEOUT"] = "1"
+    try:
+        api.forward(q, k, v, causal=True, stream=sa)
+    finally:
+        del os.environ["FA_SELFTEST_WAIT_TIMEOUT"]
+    sa.synchronize()                              # the kernel on A has finished
+    assert api.sync_status(stream=sb) == _lib.FA_ERR_TIMEOUT
+    assert api.sync_status(stream=sa) == 0        # already read and cleared via B
+    o, lse = api.forward(q, k, v, causal=True, stream=sb)
+    assert api.sync_status(stream=sb) == 0
+    compare_fwd(inp, o, lse, True, default_scale(64))

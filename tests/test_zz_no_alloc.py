@@ -67,3 +67,47 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
                              10 * fake, 12 * fake, B, H, N, 64, 0.125, 1, _lib.FA_DTYPE_BF16,
                              _lib.FA_DTYPE_BF16, None)
     assert st == _lib.FA_ERR_UNSUPPORTED
+
+
+def test_noalloc_allocates_no_device_memory():
+    """The property the entry point exists for: around warm calls (the first
+    call on a device looks up the scratch array's address), neither the
+    driver's free device memory nor torch's allocated bytes change.  The two
+    calls use 1800 and then 400 rows, so the second finds the first's larger
+    scratch contents and must not read them."""
+    torch = require_gpu()
+    from exact_attention_fwd_gb300 import _lib, api
+    dev = torch.device("cuda", 0)
+    cases = []
+    for B, H, N, causal, seed in [(2, 3, 300, True, 11010), (1, 2, 200, False, 11011)]:
+        inp = make(B, H, N, 64, "bf16", seed)
+        q, k, v, do = (inp.torch(t, dev) for t in ("q", "k", "v", "do"))
+        o, lse = api.forward(q, k, v, causal=causal)
+        ref = api.backward(q, k, v, o, lse, do, causal=causal)
+        outs = [torch.full_like(q, float("nan")) for _ in range(3)]
+        cases.append((q, k, v, o, lse, do, outs, ref, causal))
+    stream = torch.cuda.current_stream(dev).cuda_stream
+
+    def call(c):
+        q, k, v, o, lse, do, outs, _, causal = c
+        B, N, H, d = q.shape
+        st = _lib.fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), do.data_ptr(), outs[0].data_ptr(),
+                                 outs[1].data_ptr(), outs[2].data_ptr(), B, H, N, d,
+                                 1.0 / d ** 0.5, int(causal), _lib.FA_DTYPE_BF16,
+                                 _lib.FA_DTYPE_BF16, stream)
+        assert st == _lib.FA_OK, _lib.status_string(st)
+
+    call(cases[0])                        # warm
+    torch.cuda.synchronize(dev)
+    assert api.sync_status() == 0
+    free0, alloc0 = torch.cuda.mem_get_info(dev)[0], torch.cuda.memory_allocated(dev)
+    call(cases[0])
+    call(cases[1])
+    torch.cuda.synchronize(dev)
+    assert torch.cuda.mem_get_info(dev)[0] == free0
+    assert torch.cuda.memory_allocated(dev) == alloc0
+    assert api.sync_status() == 0
+    for c in cases:
+        for g, r in zip(c[6], c[7]):
+            assert float((g.float() - r.float()).abs().max()) <= TOL["bf16"]["grad"]
