@@ -18,7 +18,8 @@ EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_phase", "fa_bwd_workspace_size", "fa_sync
            "fa_status_string", "fa_bwd_noalloc", "fa_fwd_partial", "fa_merge",
            "fa_fwd_splitkv_keys_per_split", "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv",
            "fa_fwd_bwd_host_workspace_size", "fa_fwd_bwd_host", "fa_fwd_unfused_workspace_size",
-           "fa_fwd_unfused", "fa_fwd_tf32x3_workspace_size", "fa_fwd_tf32x3")
+           "fa_fwd_unfused", "fa_fwd_tf32x3_workspace_size", "fa_fwd_tf32x3",
+           "fa_bwd_tf32x3_workspace_size", "fa_bwd_tf32x3")
 FA_BWD_NOALLOC_MAX_ROWS = 1 << 22
 
 _lib = None
@@ -75,6 +76,10 @@ def load():
     lib.fa_fwd_tf32x3_workspace_size.restype = sz
     lib.fa_fwd_tf32x3.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_fwd_tf32x3.restype = i
+    lib.fa_bwd_tf32x3_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_tf32x3_workspace_size.restype = sz
+    lib.fa_bwd_tf32x3.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+    lib.fa_bwd_tf32x3.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -167,6 +172,17 @@ def fa_fwd_unfused(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, workspace,
     """The unfused comparison forward (include/fa.h)."""
     return load().fa_fwd_unfused(q, k, v, o, lse, B, H, N, d, float(scale), int(causal),
                                  int(dtype), workspace, workspace_bytes, stream)
+
+
+def fa_bwd_tf32x3_workspace_size(B, H, N, d):
+    return int(load().fa_bwd_tf32x3_workspace_size(B, H, N, d))
+
+
+def fa_bwd_tf32x3(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                  workspace_bytes, stream):
+    """float32 backward on the tensor cores (3xTF32); pointers as integers."""
+    return load().fa_bwd_tf32x3(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, float(scale),
+                                int(causal), workspace, workspace_bytes, stream)
 
 
 def fa_fwd_tf32x3_workspace_size(B, H, N, d):

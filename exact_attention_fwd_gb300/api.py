@@ -281,6 +281,33 @@ def forward_tf32x3(q, k, v, scale=None, causal=False, out=None, lse=None, ws=Non
     return out, lse
 
 
+def backward_tf32x3(q, k, v, o, lse, do, scale=None, causal=False, ws=None, dq=None, dk=None,
+                    dv=None, stream=None):
+    """float32 dQ, dK, dV on the tensor cores (fa_bwd_tf32x3, d <= 64)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check(t, name, torch.float32)
+    _check(lse, "lse", torch.float32)
+    if q.shape != k.shape or q.shape != v.shape or q.shape != o.shape or q.shape != do.shape:
+        raise ValueError("q, k, v, o, do must share one [B, N, H, d] shape")
+    B, N, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if ws is None:
+        ws = torch.empty(_lib.fa_bwd_tf32x3_workspace_size(B, H, N, d), dtype=torch.uint8,
+                         device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check(t, name, torch.float32)
+    st = _lib.fa_bwd_tf32x3(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                            dv.data_ptr(), B, H, N, d, scale, causal, ws.data_ptr(), ws.numel(),
+                            _stream_handle(stream))
+    if st != _lib.FA_OK:
+        raise _lib.FaError(st, "fa_bwd_tf32x3")
+    return dq, dk, dv
+
+
 def sync_status(stream=None):
     """Synchronise and return (and clear) the device status word."""
     return _lib.fa_sync_status(_stream_handle(stream))

@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libfa.so")
 
 SOURCES = ("fa_api.cu", "simt_f32.cu", "bwd_dot.cu", "tc_fwd.cu", "tc_bwd.cu", "fa_noalloc.cu",
            "merge.cu", "fa_host.cu", "unfused.cu",
-           "tf32x3_fwd.cu")
+           "tf32x3_fwd.cu", "tf32x3_bwd.cu")
 ARCH = ("-gencode", "arch=compute_103a,code=sm_103a")
 NVCC_FLAGS = ("-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include"))

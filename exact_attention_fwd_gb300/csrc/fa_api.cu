@@ -400,6 +400,27 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
 
 extern "C" {
 
+size_t fa_bwd_tf32x3_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  return fa::tf32x3_bwd_workspace_bytes(B, H, N, d);
+}
+
+fa_status fa_bwd_tf32x3(const float* q, const float* k, const float* v, const float* o,
+                        const float* lse, const float* dO, float* dq, float* dk, float* dv,
+                        int B, int H, int N, int d, float scale, int causal, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (d > 64 && check_shape(B, H, N, d, scale) == FA_OK) return FA_ERR_UNSUPPORTED;
+  if (workspace_bytes < fa_bwd_tf32x3_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  fa::BwdParams p;
+  fa_status st = prepare_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, FA_DTYPE_F32,
+                             FA_DTYPE_F32, workspace, workspace_bytes, &p);
+  if (st != FA_OK) return st;
+  cudaError_t e = fa::launch_bwd_tf32x3(p, workspace, static_cast<cudaStream_t>(stream),
+                                        causal != 0);
+  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 size_t fa_fwd_tf32x3_workspace_size(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
   return fa::tf32x3_workspace_bytes(B, H, N, d);

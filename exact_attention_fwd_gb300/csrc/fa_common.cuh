@@ -92,5 +92,10 @@ size_t tf32x3_workspace_bytes(int B, int H, int N, int d);
 cudaError_t launch_fwd_tf32x3(const FwdParams& p, void* workspace, cudaStream_t s, bool causal);
 // phase 1: dQ kernel (also refines D in the workspace); phase 2: dK/dV kernel.
 cudaError_t launch_bwd_tc16(const BwdParams& p, cudaStream_t s, bool causal, int phase);
+// float32 backward on the tensor cores (3xTF32), d <= 64: split passes, the D
+// pre-pass (into the workspace), the dQ kernel and the dK/dV kernel; the
+// workspace of tf32x3_bwd_workspace_bytes() holds D and the hi / lo copies
+size_t tf32x3_bwd_workspace_bytes(int B, int H, int N, int d);
+cudaError_t launch_bwd_tf32x3(const BwdParams& p, void* workspace, cudaStream_t s, bool causal);
 
 }  // namespace fa

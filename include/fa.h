@@ -360,6 +360,29 @@ fa_status fa_fwd_tf32x3(const float* q, const float* k, const float* v, float* o
 /* fa_status_string — static, human-readable name of a status code. */
 const char* fa_status_string(fa_status s);
 
+/*
+ * fa_bwd_tf32x3 — float32 backward on the tensor cores: the gradients of
+ * fa_fwd / fa_fwd_tf32x3 ("Flash Attention 2 — backward pass notes", "The
+ * math (FA2 backward with recompute)", split as option 3 of "Why the WGSL
+ * kernel isn't shipped this turn": one kernel per query tile writes dQ, one
+ * per key tile writes dK and dV, D = rowsum(dO * O) first) with every product
+ * taken as three tcgen05 kind::tf32 products of hi / lo tf32 parts
+ * (hi*hi + hi*lo + lo*hi).
+ *   q, k, v, o, dO : DEVICE, float32 [B, N, H, d], 16-byte aligned
+ *   lse            : DEVICE, float32 [B, H, N] (the forward's)
+ *   dq, dk, dv     : DEVICE, float32 [B, N, H, d], 16-byte aligned, written
+ *   d              : a multiple of 8, at most 64 (FA_ERR_UNSUPPORTED above)
+ *   workspace      : DEVICE, 256-byte aligned, >= fa_bwd_tf32x3_workspace_size
+ *                    bytes (D, the hi / lo copies of Q, K, V, dO and the
+ *                    transposed hi / lo copies of Q, K, dO); caller-owned
+ * Validation, aliasing rules, errors and the status word as fa_bwd.
+ */
+size_t fa_bwd_tf32x3_workspace_size(int B, int H, int N, int d);
+fa_status fa_bwd_tf32x3(const float* q, const float* k, const float* v, const float* o,
+                        const float* lse, const float* dO, float* dq, float* dk, float* dv,
+                        int B, int H, int N, int d, float scale, int causal, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
