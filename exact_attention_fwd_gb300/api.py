@@ -258,7 +258,7 @@ def forward_unfused(q, k, v, scale=None, causal=False, out=None, lse=None, ws=No
 
 
 def forward_tf32x3(q, k, v, scale=None, causal=False, out=None, lse=None, ws=None, stream=None):
-    """float32 O, LSE = attention(q, k, v) on the tensor cores (fa_fwd_tf32x3, d <= 64)."""
+    """float32 O, LSE = attention(q, k, v) on the tensor cores (fa_fwd_tf32x3, d <= 128)."""
     _check_qkv(q, k, v)
     if q.dtype != torch.float32:
         raise ValueError("forward_tf32x3 takes float32 tensors")

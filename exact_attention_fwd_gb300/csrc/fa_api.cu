@@ -432,7 +432,6 @@ fa_status fa_fwd_tf32x3(const float* q, const float* k, const float* v, float* o
   if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
   fa_status st = check_shape(B, H, N, d, scale);
   if (st != FA_OK) return st;
-  if (d > 64) return FA_ERR_UNSUPPORTED;
   if (workspace_bytes < fa_fwd_tf32x3_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4) || !aligned(workspace, 256))

@@ -18,18 +18,21 @@
 //      beyond N; transposed through shared-memory tiles), so that every MMA
 //      operand is K-major;
 //   2. fused pass, one CTA per (b, h, 128-row Q tile), 7 warps:
-//        warp 0 lane 0   TMA: Qh, Ql once; Kh, Kl of each 64-key block into a
-//                        3-slot ring that S frees;
-//        warp 6 lane 0   TMA: V^Th, V^Tl of each block into a 2-slot ring that
-//                        P V frees (the K loads run ahead of the V releases);
+//        warp 0 lane 0   TMA: Qh, Ql once; Kh, Kl of each key block into a
+//                        ring that S frees;
+//        warp 6 lane 0   TMA: V^Th, V^Tl of each block into a ring that P V
+//                        frees (the K loads run ahead of the V releases);
 //        warp 1 lane 0   MMAs: S = Qh Kh^T + Qh Kl^T + Ql Kh^T (fp32 in TMEM),
 //                        O += Ph Vh + Ph Vl + Pl Vh (P read from TMEM);
 //        warps 2-5       one thread per query row (TMEM lane): masked row max,
 //                        lazy rescale, P = 2^(s c - m) in float32 split into
 //                        Ph, Pl in TMEM; finally O / l and L.
-// TMEM: S [0, 64), Ph [64, 128), Pl [128, 192), O [192, 256).  S(j+1) is
-// computed while the softmax works on block j; PV(j) runs once P(j) is in
-// TMEM.  Every wait is bounded (FA_ERR_TIMEOUT, abort flag, drain).
+// Head dims up to 64 use 64-key blocks, a 3-slot K ring and a 2-slot V ring;
+// head dims up to 128 (the hi / lo Q tile then takes 128 KB) use 32-key
+// blocks, 2 K slots and 1 V slot (T3Cfg).  TMEM: S, Ph, Pl (one block's
+// keys each), then O (the padded head dim).  S(j+1) is computed while the
+// softmax works on block j; PV(j) runs once P(j) is in TMEM.  Every wait is
+// bounded (FA_ERR_TIMEOUT, abort flag, drain).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -46,32 +49,43 @@ namespace fa {
 namespace {
 
 constexpr int kBM = 128;                  // query rows per CTA
-constexpr int kBN = 64;                   // keys per block
-constexpr int kDP = 64;                   // padded head dim (d <= 64)
 constexpr int kThreads = 224;
-constexpr int kKStages = 3;               // ring of (Kh, Kl), freed when S has read it
-constexpr int kVStages = 2;               // ring of (Vh, Vl), freed when P V has read it
 constexpr int kQChunk = kBM * 128;        // 32 fp32 columns of 128 rows
-constexpr int kKChunk = kBN * 128;        // 32 fp32 columns of 64 rows
-constexpr int kQTile = 2 * kQChunk;       // 128 x 64 fp32
-constexpr int kKTile = 2 * kKChunk;       // 64 x 64 fp32
-constexpr int kOffQh = 0, kOffQl = kQTile;
-constexpr int kPairBytes = 2 * kKTile;     // one ring slot: hi tile, then lo tile
-constexpr int kOffK = 2 * kQTile;
-constexpr int kOffV = kOffK + kKStages * kPairBytes;
-constexpr int kOffBar = kOffV + kVStages * kPairBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory per block");
 constexpr int kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColPh = 64, kColPl = 128, kColO = 192;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kKStagesMax = 3, kVStagesMax = 2;
+
+// Padded head dim DP = 64: 64-key blocks, K ring 3 slots, V ring 2.
+// DP = 128: the hi / lo Q tile is 128 KB, so 32-key blocks, K ring 2 slots,
+// V ring 1 (every slot holds 16 KB hi + 16 KB lo either way).
+template <int DP>
+struct T3Cfg {
+  static constexpr int kDP = DP;
+  static constexpr int kBN = DP == 64 ? 64 : 32;          // keys per block
+  static constexpr int kKStages = DP == 64 ? 3 : 2;       // (Kh, Kl) ring, freed when S has read it
+  static constexpr int kVStages = DP == 64 ? 2 : 1;       // (V^Th, V^Tl) ring, freed by P V
+  static constexpr int kKChunk = kBN * 128;               // 32 fp32 columns of kBN rows
+  static constexpr int kVChunk = DP * 128;                // 32 keys of V^T (DP rows)
+  static constexpr int kQTile = (DP / 32) * kQChunk;      // 128 x DP fp32
+  static constexpr int kKTile = kBN * DP * 4;             // kBN x DP (= V^T's DP x kBN)
+  static constexpr int kOffQh = 0, kOffQl = kQTile;
+  static constexpr int kPairBytes = 2 * kKTile;           // one ring slot: hi tile, then lo tile
+  static constexpr int kOffK = 2 * kQTile;
+  static constexpr int kOffV = kOffK + kKStages * kPairBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kPairBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per block");
+  // TMEM: S [0, kBN), Ph [kBN, 2 kBN), Pl [2 kBN, 3 kBN), O [3 kBN, 3 kBN + DP)
+  static constexpr uint32_t kColS = 0, kColPh = kBN, kColPl = 2 * kBN, kColO = 3 * kBN;
+  static_assert(3 * kBN + DP <= kTmemCols, "TMEM columns");
+};
 
 struct Tf32Bars {
   uint64_t q_full;
-  uint64_t k_full[kKStages];
-  uint64_t k_empty[kKStages];
-  uint64_t v_full[kVStages];
-  uint64_t v_empty[kVStages];
+  uint64_t k_full[kKStagesMax];
+  uint64_t k_empty[kKStagesMax];
+  uint64_t v_full[kVStagesMax];
+  uint64_t v_empty[kVStagesMax];
   uint64_t s_full, s_free, p_full, pv_done, drain, probe;
   uint32_t tmem_base;
   int abort;
@@ -82,7 +96,7 @@ __device__ __forceinline__ void tf32_abort(Tf32Bars* bars, int* status) {
   *reinterpret_cast<volatile int*>(&bars->abort) = 1;
 }
 
-template <bool kCausal>
+template <int DP, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tf32x3_kernel(const __grid_constant__ CUtensorMap tmQh,
                       const __grid_constant__ CUtensorMap tmQl,
@@ -90,6 +104,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmKl,
                       const __grid_constant__ CUtensorMap tmVh,
                       const __grid_constant__ CUtensorMap tmVl, const FwdParams p) {
+  using Cfg = T3Cfg<DP>;
+  constexpr int kBN = Cfg::kBN, kDP = Cfg::kDP, kKStages = Cfg::kKStages,
+                kVStages = Cfg::kVStages, kKChunk = Cfg::kKChunk, kVChunk = Cfg::kVChunk,
+                kQTile = Cfg::kQTile, kKTile = Cfg::kKTile, kPairBytes = Cfg::kPairBytes;
+  constexpr int kOffQh = Cfg::kOffQh, kOffQl = Cfg::kOffQl, kOffK = Cfg::kOffK,
+                kOffV = Cfg::kOffV, kOffBar = Cfg::kOffBar;
+  constexpr uint32_t kColS = Cfg::kColS, kColPh = Cfg::kColPh, kColPl = Cfg::kColPl,
+                     kColO = Cfg::kColO;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -154,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       if (is_k) {
         mbar_arrive_expect_tx(&bars->q_full, 2 * kQTile);
-        for (int ch = 0; ch < 2; ++ch) {
+        for (int ch = 0; ch < kDP / 32; ++ch) {
           tma_load_4d(sQh + ch * kQChunk, &tmQh, &bars->q_full, ch * 32, h, qt * kBM, b);
           tma_load_4d(sQl + ch * kQChunk, &tmQl, &bars->q_full, ch * 32, h, qt * kBM, b);
         }
@@ -168,13 +190,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* slot = is_k ? kslot(s) : vslot(s);
         mbar_arrive_expect_tx(&full[s], kPairBytes);
-        for (int ch = 0; ch < 2; ++ch) {
-          if (is_k) {
+        if (is_k) {
+          for (int ch = 0; ch < kDP / 32; ++ch) {
             tma_load_4d(slot + ch * kKChunk, &tmKh, &full[s], ch * 32, h, j * kBN, b);
             tma_load_4d(slot + kKTile + ch * kKChunk, &tmKl, &full[s], ch * 32, h, j * kBN, b);
-          } else {
-            tma_load_4d(slot + ch * kKChunk, &tmVh, &full[s], j * kBN + ch * 32, 0, h, b);
-            tma_load_4d(slot + kKTile + ch * kKChunk, &tmVl, &full[s], j * kBN + ch * 32, 0, h, b);
+          }
+        } else {
+          for (int ch = 0; ch < kBN / 32; ++ch) {
+            tma_load_4d(slot + ch * kVChunk, &tmVh, &full[s], j * kBN + ch * 32, 0, h, b);
+            tma_load_4d(slot + kKTile + ch * kVChunk, &tmVl, &full[s], j * kBN + ch * 32, 0, h, b);
           }
         }
       }
@@ -189,7 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   else if (run && warp == 1) {
     // ================ MMA issuer (whole warp waits, lane 0 issues) ================
     const bool leader = lane == 0;
-    constexpr uint32_t kIdesc = idesc_tf32(kBM, kBN);   // S: N = 64 keys; PV: N = 64 columns
+    constexpr uint32_t kIdescS = idesc_tf32(kBM, kBN);   // S: N = kBN keys
+    constexpr uint32_t kIdescPV = idesc_tf32(kBM, kDP);  // PV: N = DP columns
     // K-steps over the padded head dim: columns >= d of Q and K are zero-filled
     // by the tensor maps, so a compile-time count (fully unrolled, constant
     // descriptor offsets) is exact for every d <= 64 and keeps the issuing
@@ -211,14 +236,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dVl = sdesc_sw128(smem_u32(vs + kKTile), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 8; ++kk)
-          mma_ts_tf32(tmem + kColO, tmem + kColPh + kk * 8, dVh + kstep(kk, kKChunk), kIdesc,
+          mma_ts_tf32(tmem + kColO, tmem + kColPh + kk * 8, dVh + kstep(kk, kVChunk), kIdescPV,
                       (jj > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kBN / 8; ++kk)
-          mma_ts_tf32(tmem + kColO, tmem + kColPh + kk * 8, dVl + kstep(kk, kKChunk), kIdesc, 1u);
+          mma_ts_tf32(tmem + kColO, tmem + kColPh + kk * 8, dVl + kstep(kk, kVChunk), kIdescPV, 1u);
 #pragma unroll
         for (int kk = 0; kk < kBN / 8; ++kk)
-          mma_ts_tf32(tmem + kColO, tmem + kColPl + kk * 8, dVh + kstep(kk, kKChunk), kIdesc, 1u);
+          mma_ts_tf32(tmem + kColO, tmem + kColPl + kk * 8, dVh + kstep(kk, kVChunk), kIdescPV, 1u);
         mma_commit(&bars->pv_done);
         mma_commit(&bars->v_empty[jj % kVStages]);
       }
@@ -241,14 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dKl = sdesc_sw128(smem_u32(ks + kKTile), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < nks; ++kk)
-          mma_ss_tf32(tmem + kColS, dQh + kstep(kk, kQChunk), dKh + kstep(kk, kKChunk), kIdesc,
+          mma_ss_tf32(tmem + kColS, dQh + kstep(kk, kQChunk), dKh + kstep(kk, kKChunk), kIdescS,
                       kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < nks; ++kk)
-          mma_ss_tf32(tmem + kColS, dQh + kstep(kk, kQChunk), dKl + kstep(kk, kKChunk), kIdesc, 1u);
+          mma_ss_tf32(tmem + kColS, dQh + kstep(kk, kQChunk), dKl + kstep(kk, kKChunk), kIdescS, 1u);
 #pragma unroll
         for (int kk = 0; kk < nks; ++kk)
-          mma_ss_tf32(tmem + kColS, dQl + kstep(kk, kQChunk), dKh + kstep(kk, kKChunk), kIdesc, 1u);
+          mma_ss_tf32(tmem + kColS, dQl + kstep(kk, kQChunk), dKh + kstep(kk, kKChunk), kIdescS, 1u);
         mma_commit(&bars->s_full);
         mma_commit(&bars->k_empty[s]);
       }
@@ -277,8 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       uint32_t sr[kBN];
-      tmem_ld32(tmem + lb + kColS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tmem + lb + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+#pragma unroll
+      for (int cc = 0; cc < kBN / 32; ++cc)
+        tmem_ld32(tmem + lb + kColS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
       tmem_ld_wait(sr);
       tc_fence_before();
       mbar_arrive(&bars->s_free);   // S may take the next block's scores
@@ -336,10 +362,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      tmem_st32(tmem + lb + kColPh, *reinterpret_cast<uint32_t(*)[32]>(&ph[0]));
-      tmem_st32(tmem + lb + kColPh + 32, *reinterpret_cast<uint32_t(*)[32]>(&ph[32]));
-      tmem_st32(tmem + lb + kColPl, *reinterpret_cast<uint32_t(*)[32]>(&pl[0]));
-      tmem_st32(tmem + lb + kColPl + 32, *reinterpret_cast<uint32_t(*)[32]>(&pl[32]));
+#pragma unroll
+      for (int cc = 0; cc < kBN / 32; ++cc) {
+        tmem_st32(tmem + lb + kColPh + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&ph[cc * 32]));
+        tmem_st32(tmem + lb + kColPl + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&pl[cc * 32]));
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p_full);
@@ -411,9 +438,12 @@ size_t tf32x3_workspace_bytes(int B, int H, int N, int d) {
   return 4 * a + 2 * t;
 }
 
-cudaError_t launch_fwd_tf32x3(const FwdParams& p, void* workspace, cudaStream_t st, bool causal) {
+namespace {
+
+template <int DP>
+cudaError_t launch_t3(const FwdParams& p, void* workspace, cudaStream_t st, bool causal) {
+  using Cfg = T3Cfg<DP>;
   const int B = p.B, H = p.H, N = p.N, d = p.d, Np = round4(N);
-  if (d > kDP || d % 8 != 0) return cudaErrorNotSupported;
   const size_t a = (static_cast<size_t>(B) * N * H * d * 4 + 255) & ~static_cast<size_t>(255);
   const size_t t = (static_cast<size_t>(B) * H * d * Np * 4 + 255) & ~static_cast<size_t>(255);
   char* w = static_cast<char*>(workspace);
@@ -430,8 +460,8 @@ cudaError_t launch_fwd_tf32x3(const FwdParams& p, void* workspace, cudaStream_t 
   const cuuint64_t sv[3] = {static_cast<cuuint64_t>(Np) * 4, static_cast<cuuint64_t>(d) * Np * 4,
                             static_cast<cuuint64_t>(H) * d * Np * 4};
   const cuuint32_t box_q[4] = {32u, 1u, static_cast<cuuint32_t>(kBM), 1u};
-  const cuuint32_t box_k[4] = {32u, 1u, static_cast<cuuint32_t>(kBN), 1u};
-  const cuuint32_t box_v[4] = {32u, static_cast<cuuint32_t>(kDP), 1u, 1u};
+  const cuuint32_t box_k[4] = {32u, 1u, static_cast<cuuint32_t>(Cfg::kBN), 1u};
+  const cuuint32_t box_v[4] = {32u, static_cast<cuuint32_t>(DP), 1u, 1u};
   CUtensorMap mqh, mql, mkh, mkl, mvh, mvl;
   cudaError_t e = make_f32_tmap(&mqh, qh, dq, sq, box_q);
   if (e == cudaSuccess) e = make_f32_tmap(&mql, ql, dq, sq, box_q);
@@ -461,13 +491,21 @@ cudaError_t launch_fwd_tf32x3(const FwdParams& p, void* workspace, cudaStream_t 
   if (e != cudaSuccess) return e;
   const long long ctas = static_cast<long long>(B) * H * ((N + kBM - 1) / kBM);
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  auto kern = causal ? fwd_tf32x3_kernel<true> : fwd_tf32x3_kernel<false>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  auto kern = causal ? fwd_tf32x3_kernel<DP, true> : fwd_tf32x3_kernel<DP, false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   FwdParams pc = p;
   void* args[] = {&mqh, &mql, &mkh, &mkl, &mvh, &mvl, &pc};
   return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(static_cast<unsigned>(ctas)),
-                          dim3(kThreads), args, kSmemBytes, st);
+                          dim3(kThreads), args, Cfg::kSmemBytes, st);
 }
+
+}  // namespace
+
+cudaError_t launch_fwd_tf32x3(const FwdParams& p, void* workspace, cudaStream_t st, bool causal) {
+  if (p.d % 8 != 0 || p.d > 128) return cudaErrorNotSupported;
+  return p.d <= 64 ? launch_t3<64>(p, workspace, st, causal) : launch_t3<128>(p, workspace, st, causal);
+}
+
 
 }  // namespace fa

@@ -346,7 +346,9 @@ fa_status fa_fwd_unfused(const void* q, const void* k, const void* v, void* o, f
  *
  *   q, k, v   in : [B, N, H, d] float32
  *   o        out : [B, N, H, d] float32;  lse out : [B, H, N] float32
- *   d            : a multiple of 8 in [8, 64] (d > 64: FA_ERR_UNSUPPORTED)
+ *   d            : a multiple of 8 in [8, 128]; d <= 64 runs 64-key blocks,
+ *                  d in (64, 128] 32-key blocks (the hi/lo Q tile of 128
+ *                  rows then takes 128 KB of shared memory)
  *   workspace    : DEVICE, 256-byte aligned, >= fa_fwd_tf32x3_workspace_size
  *                  (B, H, N, d) bytes: the hi/lo split of q, k and v (v
  *                  transposed per head), 6 float32 copies of an input

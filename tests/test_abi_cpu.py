@@ -17,6 +17,21 @@ def lib():
     return _lib.load()
 
 
+@pytest.fixture(scope="module")
+def fake_lib(lib):
+    """The library, for calls with fake device addresses that validation must
+    reject before any launch.  Skipped where a CUDA device is visible: if a
+    case ever passed validation there, its kernels would touch the fake
+    addresses."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("fake device addresses are only passed where no GPU is visible")
+    except ImportError:
+        pass
+    return lib
+
+
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "fa.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
@@ -59,7 +74,7 @@ FAKE = 1 << 20   # 16-byte aligned address; validation fails before any use
     (dict(q=FAKE + 8), 1),                 # misaligned
     (dict(o=FAKE), 1),                     # output aliases q
 ])
-def test_fwd_rejects_invalid_arguments(lib, kw, want):
+def test_fwd_rejects_invalid_arguments(fake_lib, kw, want):
     from exact_attention_fwd_gb300 import _lib
     a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, B=1, H=1, N=16, d=64,
              scale=0.125, causal=1, dtype=1, stream=None)
@@ -77,7 +92,7 @@ def test_fwd_rejects_invalid_arguments(lib, kw, want):
     (dict(dk=8 * FAKE), 1),                # aliases dq
     (dict(workspace=FAKE + 16), 1),        # not 256-byte aligned (and aliases)
 ])
-def test_bwd_rejects_invalid_arguments(lib, kw, want):
+def test_bwd_rejects_invalid_arguments(fake_lib, kw, want):
     from exact_attention_fwd_gb300 import _lib
     a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, dO=6 * FAKE,
              dq=8 * FAKE, dk=10 * FAKE, dv=12 * FAKE, B=1, H=1, N=16, d=64, scale=0.125,
@@ -87,7 +102,7 @@ def test_bwd_rejects_invalid_arguments(lib, kw, want):
     assert _lib.fa_bwd(**a) == want
 
 
-def test_bwd_phase_rejects_bad_phase(lib):
+def test_bwd_phase_rejects_bad_phase(fake_lib):
     from exact_attention_fwd_gb300 import _lib
     a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, dO=6 * FAKE,
              dq=8 * FAKE, dk=10 * FAKE, dv=12 * FAKE, B=1, H=1, N=16, d=64, scale=0.125,
@@ -121,7 +136,7 @@ def test_splitkv_sizes(lib):
     (dict(o_part=FAKE), 1),                # overlaps q
     (dict(lse_part=4 * FAKE + 64), 1),     # overlaps o_part
 ])
-def test_fwd_partial_rejects_invalid_arguments(lib, kw, want):
+def test_fwd_partial_rejects_invalid_arguments(fake_lib, kw, want):
     from exact_attention_fwd_gb300 import _lib
     a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o_part=4 * FAKE, lse_part=8 * FAKE, B=1, H=1, N=16,
              d=64, scale=0.125, causal=1, dtype=1, keys_per_split=256, stream=None)
@@ -137,7 +152,7 @@ def test_fwd_partial_rejects_invalid_arguments(lib, kw, want):
     (dict(o=FAKE + 64), 1),                # overlaps o_part
     (dict(N=0), 1),
 ])
-def test_merge_rejects_invalid_arguments(lib, kw, want):
+def test_merge_rejects_invalid_arguments(fake_lib, kw, want):
     from exact_attention_fwd_gb300 import _lib
     a = dict(o_part=FAKE, lse_part=2 * FAKE, num_splits=2, keys_per_split=256, causal=1,
              o=4 * FAKE, lse=5 * FAKE, B=1, H=1, N=16, d=64, dtype=1, stream=None)
@@ -153,7 +168,7 @@ def test_merge_rejects_invalid_arguments(lib, kw, want):
     (dict(workspace=FAKE), 1),             # overlaps q
     (dict(dtype=0), 2),
 ])
-def test_splitkv_rejects_invalid_arguments(lib, kw, want):
+def test_splitkv_rejects_invalid_arguments(fake_lib, kw, want):
     from exact_attention_fwd_gb300 import _lib
     a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, B=1, H=1, N=16, d=64,
              scale=0.125, causal=1, dtype=1, num_splits=2, workspace=8 * FAKE,
@@ -184,7 +199,7 @@ def test_host_workspace_size(lib):
     (dict(scale=float("nan")), 1),
     (dict(grad_dtype=2), 1),
 ])
-def test_host_rejects_invalid_arguments(lib, kw, want):
+def test_host_rejects_invalid_arguments(fake_lib, kw, want):
     from exact_attention_fwd_gb300 import _lib
     a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, dO=4 * FAKE, o=5 * FAKE, lse=6 * FAKE, dq=7 * FAKE,
              dk=8 * FAKE, dv=9 * FAKE, B=4, H=2, N=16, d=64, scale=0.125, causal=1, dtype=1,
@@ -212,7 +227,7 @@ def test_unfused_workspace_size(lib):
     (dict(q=FAKE + 4), 1),                  # misaligned
     (dict(scale=float("inf")), 1),
 ])
-def test_unfused_rejects_invalid_arguments(lib, kw, want):
+def test_unfused_rejects_invalid_arguments(fake_lib, kw, want):
     from exact_attention_fwd_gb300 import _lib
     a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, B=1, H=1, N=16, d=64,
              scale=0.125, causal=1, dtype=1, workspace=16 * FAKE, workspace_bytes=1 << 26,
@@ -231,13 +246,13 @@ def test_tf32x3_workspace_size(lib):
 
 @pytest.mark.parametrize("kw,want", [
     (dict(q=0), 1), (dict(workspace=0), 1),
-    (dict(d=72), 2), (dict(d=136), 2), (dict(d=12), 1),
+    (dict(d=136), 2), (dict(d=12), 1),
     (dict(workspace_bytes=100), 1),
     (dict(workspace=16 * FAKE + 64), 1),
     (dict(o=FAKE), 1),                     # aliases q
     (dict(scale=float("nan")), 1),
 ])
-def test_tf32x3_rejects_invalid_arguments(lib, kw, want):
+def test_tf32x3_rejects_invalid_arguments(fake_lib, kw, want):
     from exact_attention_fwd_gb300 import _lib
     a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, B=1, H=1, N=16, d=64,
              scale=0.125, causal=1, workspace=16 * FAKE, workspace_bytes=1 << 22, stream=None)
@@ -256,3 +271,20 @@ def test_missing_library_raises(monkeypatch, tmp_path):
                  lambda: _lib.fa_fwd_unfused_workspace_size(1, 1, 128, 64)):
         with pytest.raises(RuntimeError, match="not built"):
             call()
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), 1), (dict(workspace=0), 1),
+    (dict(d=72), 2),                       # the 3xTF32 backward takes d <= 64
+    (dict(d=12), 1),
+    (dict(workspace_bytes=100), 1),
+    (dict(dq=FAKE), 1),                    # aliases q
+    (dict(scale=float("nan")), 1),
+])
+def test_bwd_tf32x3_rejects_invalid_arguments(fake_lib, kw, want):
+    from exact_attention_fwd_gb300 import _lib
+    a = dict(q=FAKE, k=2 * FAKE, v=3 * FAKE, o=4 * FAKE, lse=5 * FAKE, dO=6 * FAKE,
+             dq=8 * FAKE, dk=10 * FAKE, dv=12 * FAKE, B=1, H=1, N=16, d=64, scale=0.125,
+             causal=1, workspace=16 * FAKE, workspace_bytes=1 << 24, stream=None)
+    a.update(kw)
+    assert _lib.fa_bwd_tf32x3(**a) == want

@@ -25,8 +25,6 @@ def test_causal_sweep_tf32x3(sub):
     require_gpu()
     w = WORKLOADS[1]
     s = w.shapes[sub]
-    if s.d > 64:
-        pytest.skip("d > 64 is not on this path")
     inp = make(s.B, s.H, s.N, s.d, "f32", w.seed(sub))
     o, lse = _run(inp, True, w.scale(s))
     compare_fwd(inp, o, lse, True, w.scale(s))
@@ -36,6 +34,8 @@ def test_causal_sweep_tf32x3(sub):
 @pytest.mark.parametrize("B,H,N,d", [
     (1, 1, 64, 16), (2, 2, 300, 64), (1, 3, 129, 32), (1, 2, 1, 8), (2, 1, 257, 40),
     (1, 2, 1024, 64),
+    # head dims past 64: 32-key blocks with the 128-column padded tile
+    (1, 2, 300, 128), (2, 1, 257, 96), (1, 2, 1, 128), (1, 1, 640, 72), (1, 2, 1024, 128),
 ])
 def test_shapes_tf32x3(B, H, N, d, causal):
     require_gpu()
