@@ -15,6 +15,9 @@ forward):
   ``forward_unfused`` per repetition;
 * ``tf32x3``: B8 H16 N1024 d64 causal float32, ``forward_tf32x3`` (split pass
   plus one tensor-core kernel);
+* ``tf32x3_bwd``: B8 H16 N1024 d64 causal float32, ``backward_tf32x3`` (split
+  passes, the D pre-pass, the dQ kernel and the dK/dV kernel; FLOP 2.5 times
+  the forward's);
 * ``splitkv``: B1 H1 N32768 d128 causal bf16, ``forward_splitkv`` with 8 key
   slices (partial forward plus merge);
 * ``bert_fwd`` / ``bert_bwd``: B64 H16 N512 d64 non-causal bf16, Q and K with
@@ -75,6 +78,17 @@ def _case_tf32x3(dev):
         lambda: api.forward_tf32x3(q, k, v, causal=True, out=o, lse=lse, ws=ws)
 
 
+def _case_tf32x3_bwd(dev):
+    B, H, N, d = 8, 16, 1024, 64
+    q, k, v, do = _inputs((B, N, H, d), torch.float32, dev, count=4)
+    o, lse = api.forward(q, k, v, causal=True)
+    ws = torch.empty(api._lib.fa_bwd_tf32x3_workspace_size(B, H, N, d), dtype=torch.uint8,
+                     device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    return (B, H, N, d), 2.5 * 4.0 * B * H * d * _pairs(N, True), \
+        lambda: api.backward_tf32x3(q, k, v, o, lse, do, causal=True, ws=ws, dq=dq, dk=dk, dv=dv)
+
+
 def _case_splitkv(dev):
     B, H, N, d, S = 1, 1, 32768, 128, 8
     q, k, v = _inputs((B, N, H, d), torch.bfloat16, dev)
@@ -105,6 +119,7 @@ CASES = {
     "long_fwd": _case_long_fwd,
     "gpt2_unfused": _case_gpt2_unfused,
     "tf32x3": _case_tf32x3,
+    "tf32x3_bwd": _case_tf32x3_bwd,
     "splitkv": _case_splitkv,
     "bert_fwd": lambda dev: _fwd_bwd_pair(64, 16, 512, 64, False, 4.0, dev, False),
     "bert_bwd": lambda dev: _fwd_bwd_pair(64, 16, 512, 64, False, 4.0, dev, True),

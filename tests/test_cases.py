@@ -11,7 +11,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_case_registry_matches_documented_names():
     assert sorted(cases.CASES) == ["bert_bwd", "bert_fwd", "gpt2_unfused", "long4_bwd",
-                                   "long4_fwd", "long_fwd", "splitkv", "tf32x3"]
+                                   "long4_fwd", "long_fwd", "splitkv", "tf32x3", "tf32x3_bwd"]
     doc = cases.__doc__
     for name in cases.CASES:
         assert f"``{name}``" in doc

@@ -12,7 +12,7 @@ import pytest
 
 from exact_attention_fwd_gb300 import build
 
-SOURCES = ("tc_fwd.cu", "tc_bwd.cu", "tf32x3_fwd.cu")
+SOURCES = ("tc_fwd.cu", "tc_bwd.cu", "tf32x3_fwd.cu", "tf32x3_bwd.cu")
 
 # (kernel, template arguments as digits) with known, tolerated spills
 #   fwd_tc_kernel<DP, causal, f16, split>, bwd_tc_kernel<DP, causal, dKdV, f32grad, f16>
@@ -78,18 +78,24 @@ def spill_rows(tmp_path_factory):
 
 def test_every_kernel_reported(spill_rows):
     names = {r[0] for r in spill_rows}
-    for k in ("fwd_tc_kernel", "bwd_tc_kernel", "fwd_tf32x3_kernel", "split_qk_kernel",
-              "split_vt_kernel"):
+    for k in ("fwd_tc_kernel", "bwd_tc_kernel", "fwd_tf32x3_kernel", "bwd_tf32x3_kernel",
+              "split_qk_kernel", "split_vt_kernel"):
         assert k in names
-    # 16 forward and 32 backward instantiations
+    # 16 forward and 32 backward instantiations; 3xTF32: 4 forward (DP, causal) and 4
+    # backward (dK/dV, causal)
     assert sum(r[0] == "fwd_tc_kernel" for r in spill_rows) == 16
     assert sum(r[0] == "bwd_tc_kernel" for r in spill_rows) == 32
+    assert sum(r[0] == "fwd_tf32x3_kernel" for r in spill_rows) == 4
+    assert sum(r[0] == "bwd_tf32x3_kernel" for r in spill_rows) == 4
 
 
 def test_hot_path_does_not_spill(spill_rows):
     hot = {("fwd_tc_kernel", "64,1,0,0"), ("fwd_tc_kernel", "128,1,0,0"),
            ("bwd_tc_kernel", "64,1,0,0,0"), ("bwd_tc_kernel", "64,1,1,0,0"),
-           ("fwd_tf32x3_kernel", "1"), ("fwd_tf32x3_kernel", "0")}
+           ("fwd_tf32x3_kernel", "64,1"), ("fwd_tf32x3_kernel", "64,0"),
+           ("fwd_tf32x3_kernel", "128,1"), ("fwd_tf32x3_kernel", "128,0"),
+           ("bwd_tf32x3_kernel", "0,1"), ("bwd_tf32x3_kernel", "1,1"),
+           ("bwd_tf32x3_kernel", "0,0"), ("bwd_tf32x3_kernel", "1,0")}
     seen = set()
     for name, args, st, ld in spill_rows:
         if (name, args) in hot:
