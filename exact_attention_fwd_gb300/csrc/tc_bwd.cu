@@ -372,6 +372,78 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   constexpr int kVecs = Cfg::kBlkTile / 16;   // 16-byte units of a C1 tile
 
+  // dK/dV kernel: the per-query -L2 and -D of each streamed block, written
+  // to the stage by one warp.  L and D of a block are read one block ahead,
+  // as two independent loads, and stored in their own part of the stage
+  // (which TMA does not write) as soon as the stage's previous round has
+  // been released, so the warp runs up to a ring's depth ahead of the
+  // element-wise warps.  Returns false if a wait gave up.
+  auto vec_loader = [&]() -> bool {
+    int c = 0, li = 0;
+    bool ok = true;
+    constexpr int U = kBlk / 32;
+    auto load = [&](const Item& wi, int ti, float (&L)[U], float (&Dv)[U]) {
+      const size_t hb = (static_cast<size_t>(wi.b) * H + wi.h) * N;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int q = (wi.i0 + ti) * kBlk + u * 32 + lane;
+        L[u] = -INFINITY;   // padded query: P = 0
+        Dv[u] = 0.0f;
+        if (q < N) {
+          L[u] = p.lse[hb + q];
+          Dv[u] = p.D[hb + q];
+        }
+      }
+    };
+    int it = item_index(0, num_items);
+    Item w{};
+    int t = 0;
+    float cl[U], cd[U];
+    if (it >= 0) {
+      w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
+      load(w, 0, cl, cd);
+    }
+    while (it >= 0) {
+      // the next block (possibly the next item's first)
+      Item wn = w;
+      int tn = t + 1, itn = it, lin = li;
+      if (tn >= w.nb) {
+        lin = li + 1;
+        itn = item_index(lin, num_items);
+        tn = 0;
+        if (itn >= 0) wn = decode_item<kDkDv, kCausal, kBlk>(itn, N, H);
+      }
+      float nl[U], nd[U];
+      if (itn >= 0) load(wn, tn, nl, nd);
+      const int s = c % S, round = c / S;
+      if (round > 0 &&
+          !warp_wait(&bars->c_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
+        ok = false;
+        break;
+      }
+      float* vec = stage_vec(s);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        // a fully masked query (L = -inf) gets P = 0 and dS = 0
+        const bool live = cl[u] != -INFINITY;
+        vec[u * 32 + lane] = live ? -cl[u] * kLog2e : -INFINITY;   // -L2: exponent s c + (-L2)
+        vec[kBlk + u * 32 + lane] = live ? -cd[u] : 0.0f;          // -D
+      }
+      mbar_arrive(&bars->vec_full[s]);
+      ++c;
+      w = wn;
+      t = tn;
+      it = itn;
+      li = lin;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        cl[u] = nl[u];
+        cd[u] = nd[u];
+      }
+    }
+    return ok;
+  };
+
   // Role bodies; each runs inside the branch that sets its register budget
   // (setmaxnreg: the element-wise warps hold S, dP, P and dS of a row).
   auto helper_roles = [&]() {
@@ -698,90 +770,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (run && warp == 2) {
     // ===== narrow layout: per-query L and D of each streamed block (dK/dV) =====
-    if (kDkDv) {
-      int c = 0, li = 0;
-      bool ok = true;
-      for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
-        const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
-        const size_t hb = (static_cast<size_t>(w.b) * H + w.h) * N;
-        for (int t = 0; t < w.nb; ++t, ++c) {
-          const int s = c % S, round = c / S;
-          if (round > 0 &&
-              !warp_wait(&bars->c_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
-            ok = false;
-            break;
-          }
-          float* vec = stage_vec(s);
-#pragma unroll
-          for (int u = 0; u < kBlk / 32; ++u) {
-            const int col = u * 32 + lane;
-            const int q = (w.i0 + t) * kBlk + col;
-            float l2 = INFINITY, dd = 0.0f;   // padded or fully masked query: P = 0
-            if (q < N) {
-              const float L = p.lse[hb + q];
-              if (L != -INFINITY) {
-                l2 = L * kLog2e;
-                dd = p.D[hb + q];
-              }
-            }
-            vec[col] = -l2;          // stored negated: the exponent is s c + (-L2)
-            vec[kBlk + col] = -dd;
-          }
-          mbar_arrive(&bars->vec_full[s]);
-        }
-      }
-      if (!ok && lane == 0) raise_abort(bars, p.status);
-    }
+    if (kDkDv && !vec_loader() && lane == 0) raise_abort(bars, p.status);
     __syncwarp();
   } else if (run && warp == 3) {
     // ============ fp16 copy of each streamed C1 tile (same swizzled layout) ============
-    // Narrow layout: the whole copy.  dK/dV, wide: no copy (the element-wise
-    // warps make it), but the per-query -L2 and -D of each block (read from
-    // global memory before the block has landed).  dQ, wide: the second half
-    // (warp 2 makes the first); with kThree warp 3 is the third MMA issuer
-    // and makes that half there.
+    // Narrow layout: the whole copy.  dQ, wide: the second half (warp 2 makes
+    // the first); with kThree warp 3 is the third MMA issuer and makes that
+    // half there.  dK/dV, wide: no copy (the element-wise warps make it), but
+    // the per-query -L2 and -D of each block.
     constexpr bool kVec = kWide && kDkDv;
     int c = 0, li = 0;
     bool ok = true;
-    for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
-      const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
-      const size_t hb = (static_cast<size_t>(w.b) * H + w.h) * N;
-      for (int t = 0; t < w.nb; ++t, ++c) {
-        const int s = c % S;
-        float nl2[kBlk / 32], nd[kBlk / 32];
-        if constexpr (kVec) {
-#pragma unroll
-          for (int u = 0; u < kBlk / 32; ++u) {
-            const int q = (w.i0 + t) * kBlk + u * 32 + lane;
-            float l2 = INFINITY, dd = 0.0f;   // padded or fully masked query: P = 0
-            if (q < N) {
-              const float L = p.lse[hb + q];
-              if (L != -INFINITY) {
-                l2 = L * kLog2e;
-                dd = p.D[hb + q];
-              }
-            }
-            nl2[u] = -l2;   // stored negated: the exponent is s c + (-L2)
-            nd[u] = -dd;
+    if constexpr (kVec) {
+      ok = vec_loader();
+    } else {
+      for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
+        const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
+        for (int t = 0; t < w.nb; ++t, ++c) {
+          const int s = c % S;
+          if (!warp_wait(&bars->c_full[s], (c / S) & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
           }
+          if (kF16) continue;   // fp16 storage: the tile itself is the operand
+          convert_c1(s, kWide ? kVecs / 2 : 0, kVecs, lane, 32);
+          mbar_arrive(&bars->conv_full[s]);
         }
-        if (!warp_wait(&bars->c_full[s], (c / S) & 1, abort_flag, kWaitBudget)) {
-          ok = false;
-          break;
-        }
-        if constexpr (kVec) {
-          float* vec = stage_vec(s);
-#pragma unroll
-          for (int u = 0; u < kBlk / 32; ++u) {
-            vec[u * 32 + lane] = nl2[u];
-            vec[kBlk + u * 32 + lane] = nd[u];
-          }
-          mbar_arrive(&bars->vec_full[s]);
-        }
-        if (kWide && kDkDv) continue;   // the element-wise warps make this copy
-        if (kF16) continue;   // fp16 storage: the tile itself is the operand
-        convert_c1(s, kWide ? kVecs / 2 : 0, kVecs, lane, 32);
-        mbar_arrive(&bars->conv_full[s]);
       }
     }
     if (!ok && lane == 0) raise_abort(bars, p.status);
@@ -816,18 +830,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     bool ok = true;
+    // dQ kernel: this thread's query L and D of an item, read one item ahead
+    // (two independent loads) so the first block's exponent does not wait
+    auto load_row = [&](int it2, float& L, float& Dv) {
+      L = -INFINITY;
+      Dv = 0.0f;
+      if (it2 < 0) return;
+      const Item w2 = decode_item<kDkDv, kCausal, kBlk>(it2, N, H);
+      const int g2 = w2.row0 + row;
+      if (g2 < N) {
+        const size_t hb2 = (static_cast<size_t>(w2.b) * H + w2.h) * N;
+        L = p.lse[hb2 + g2];
+        Dv = p.D[hb2 + g2];
+      }
+    };
+    float L_nx = -INFINITY, D_nx = 0.0f;
+    if (!kDkDv) load_row(item_index(0, num_items), L_nx, D_nx);
     for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
       const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
       const int grow = w.row0 + row;      // query (dQ) or key (dK/dV)
       const size_t hb = (static_cast<size_t>(w.b) * H + w.h) * N;
       float l2_row = INFINITY, d_row = 0.0f;          // dQ kernel: this query's L, D~
       bool live_row = false;
-      if (!kDkDv && grow < N) {
-        const float L = p.lse[hb + grow];
-        if (L != -INFINITY) {
+      if (!kDkDv) {
+        const float L = L_nx, Dv = D_nx;
+        load_row(item_index(li + 1, num_items), L_nx, D_nx);
+        if (grow < N && L != -INFINITY) {
           live_row = true;
           l2_row = L * kLog2e;
-          d_row = p.D[hb + grow];
+          d_row = Dv;
         }
       }
       float d_acc = 0.0f;                             // dQ kernel: sum_j P_ij dP_ij
