@@ -279,10 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmG1, const __grid_constant__ CUtensorMap tmG2,
                   const BwdParams p) {
   using Cfg = BwdCfg<DP>;
-  // S/dP, acc1 and acc2 from three issuing warps (1, 3, 2): the causal dQ
-  // kernel only; elsewhere the third issuer's state pushes the 88-register
-  // helper warps into spills, and warp 1 issues S/dP and acc1
-  constexpr bool kThree = Cfg::kWide && !kDkDv && kCausal;
+  // S/dP, acc1 and acc2 from three issuing warps (1, 3, 2): the wide dQ
+  // kernel (its fp16 copy of K is made by the element-wise warps, so warps 2
+  // and 3 only issue); in the dK/dV kernel the third issuer's state pushes
+  // the 88-register helper warps into spills, and warp 1 issues S/dP and acc1
+  constexpr bool kThree = Cfg::kWide && !kDkDv;
   constexpr int S = Cfg::kStages;
   constexpr int kBlk = Cfg::kBlk;
   constexpr bool kWide = Cfg::kWide;
@@ -306,9 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->c_full[s], 1);
       mbar_init(&bars->c_empty[s], kWide ? 2 : 1);   // one commit per MMA warp
       mbar_init(&bars->vec_full[s], 32);
-      // who makes the fp16 copy: dK/dV wide: the 256 element-wise threads;
-      // dQ wide: warps 2 and 3 (half each); narrow: warp 3
-      mbar_init(&bars->conv_full[s], kWide ? (kDkDv ? 256 : 64) : 32);
+      // who makes the fp16 copy: wide layout: the 256 element-wise threads;
+      // narrow: warp 3
+      mbar_init(&bars->conv_full[s], kWide ? 256 : 32);
     }
     mbar_init(&bars->sp_full, 1);
     mbar_init(&bars->sp_free, 256);
@@ -600,60 +601,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
       const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
       if (kThree && warp == 3) {
-        // third MMA warp (causal dQ kernel): the acc1 accumulations of every block.
-        // Before waiting for a block's P and dS it prepares the next block:
-        // the per-query -L2 and -D (dK/dV) or the second half of the fp16
-        // copy of C1 (dQ), so the element-wise warps do not wait for them.
-        // S/dP (warp 1), acc1 (warp 3) and acc2 (warp 2) come from three
-        // threads, so no chain of MMAs waits behind another in program order.
-        const size_t hb = (static_cast<size_t>(w.b) * H + w.h) * N;
-        auto prep = [&](int t) -> bool {
-          const int cb = c + t, s = cb % S;
-          if constexpr (kDkDv) {
-            float nl2[kBlk / 32], nd[kBlk / 32];
-#pragma unroll
-            for (int u = 0; u < kBlk / 32; ++u) {
-              const int q = (w.i0 + t) * kBlk + u * 32 + lane;
-              float l2 = INFINITY, dd = 0.0f;   // padded or fully masked query: P = 0
-              if (q < N) {
-                const float L = p.lse[hb + q];
-                if (L != -INFINITY) {
-                  l2 = L * kLog2e;
-                  dd = p.D[hb + q];
-                }
-              }
-              nl2[u] = -l2;   // stored negated: the exponent is s c + (-L2)
-              nd[u] = -dd;
-            }
-            if (!wait_c(cb)) return false;
-            float* vec = stage_vec(s);
-#pragma unroll
-            for (int u = 0; u < kBlk / 32; ++u) {
-              vec[u * 32 + lane] = nl2[u];
-              vec[kBlk + u * 32 + lane] = nd[u];
-            }
-            mbar_arrive(&bars->vec_full[s]);
-          } else {
-            if (!wait_c(cb)) return false;
-            if (!kF16) {
-              convert_c1(s, kVecs / 2, kVecs, lane, 32);
-              mbar_arrive(&bars->conv_full[s]);
-            }
-          }
-          return true;
-        };
-        if (w.nb > 0 && !prep(0)) {
-          ok = false;
-          break;
-        }
+        // third MMA warp (causal dQ kernel): the acc1 accumulations of every
+        // block.  S/dP (warp 1), acc1 (warp 3) and acc2 (warp 2) come from
+        // three threads, so no chain of MMAs waits behind another in program
+        // order.
         for (int t = 0; t < w.nb; ++t) {
           const int cb = c + t;
-          if (t + 1 < w.nb && !prep(t + 1)) {
-            ok = false;
-            break;
-          }
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
-              !wait_acc_inputs(cb, t == 0, li, !kDkDv)) {
+              !wait_acc_inputs(cb, t == 0, li)) {
             ok = false;
             break;
           }
@@ -673,16 +628,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with N = 64 MMAs)
         for (int t = 0; t < w.nb; ++t) {
           const int cb = c + t;
-          if (!kDkDv) {   // dQ: first half of the block's fp16 copy (warp 3 the second)
-            if (!wait_c(cb)) {
-              ok = false;
-              break;
-            }
-            if (!kF16) {
-              convert_c1(cb % S, 0, kVecs / 2, lane, 32);
-              mbar_arrive(&bars->conv_full[cb % S]);
-            }
-          }
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
               !wait_acc_inputs(cb, t == 0, li)) {
             ok = false;
@@ -774,16 +719,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (run && warp == 3) {
     // ============ fp16 copy of each streamed C1 tile (same swizzled layout) ============
-    // Narrow layout: the whole copy.  dQ, wide: the second half (warp 2 makes
-    // the first); with kThree warp 3 is the third MMA issuer and makes that
-    // half there.  dK/dV, wide: no copy (the element-wise warps make it), but
-    // the per-query -L2 and -D of each block.
-    constexpr bool kVec = kWide && kDkDv;
+    // Narrow layout: the whole copy.  Wide layout: no copy (the element-wise
+    // warps make it); in the dK/dV kernel the per-query -L2 and -D of each
+    // block; in the dQ kernel nothing (with kThree this warp is the third
+    // MMA issuer, above).
     int c = 0, li = 0;
     bool ok = true;
-    if constexpr (kVec) {
+    if constexpr (kWide && kDkDv) {
       ok = vec_loader();
-    } else {
+    } else if constexpr (!kWide) {
       for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
         const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
         for (int t = 0; t < w.nb; ++t, ++c) {
@@ -976,6 +920,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_ld32(tdP, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
         tmem_ld32(tdP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+        // wide dQ kernel: this block's fp16 copy of K for the accumulations
+        // (the block has landed: its S was computed), made while the loads
+        // are in flight and off the MMA-issuing warps
+        if (kWide && !kDkDv && !kF16) {
+          convert_c1(s, 0, kVecs, threadIdx.x - 128, 256);
+          mbar_arrive(&bars->conv_full[s]);
+        }
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
         if (kWide) {
