@@ -280,10 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const BwdParams p) {
   using Cfg = BwdCfg<DP>;
   // S/dP, acc1 and acc2 from three issuing warps (1, 3, 2): the wide dQ
-  // kernel (its fp16 copy of K is made by the element-wise warps, so warps 2
-  // and 3 only issue); in the dK/dV kernel the third issuer's state pushes
-  // the 88-register helper warps into spills, and warp 1 issues S/dP and acc1
-  constexpr bool kThree = Cfg::kWide && !kDkDv;
+  // kernels and the causal wide dK/dV kernel (the fp16 copies are made by the
+  // element-wise warps; in that dK/dV kernel warp 2 also writes the
+  // per-query vectors).  The non-causal dK/dV kernel measured faster with
+  // two (warp 1: S/dP and acc1) and warp 3 writing the vectors.
+  constexpr bool kThree = Cfg::kWide && (!kDkDv || kCausal);
   constexpr int S = Cfg::kStages;
   constexpr int kBlk = Cfg::kBlk;
   constexpr bool kWide = Cfg::kWide;
@@ -374,75 +375,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kVecs = Cfg::kBlkTile / 16;   // 16-byte units of a C1 tile
 
   // dK/dV kernel: the per-query -L2 and -D of each streamed block, written
-  // to the stage by one warp.  L and D of a block are read one block ahead,
-  // as two independent loads, and stored in their own part of the stage
-  // (which TMA does not write) as soon as the stage's previous round has
-  // been released, so the warp runs up to a ring's depth ahead of the
-  // element-wise warps.  Returns false if a wait gave up.
-  auto vec_loader = [&]() -> bool {
-    int c = 0, li = 0;
-    bool ok = true;
-    constexpr int U = kBlk / 32;
-    auto load = [&](const Item& wi, int ti, float (&L)[U], float (&Dv)[U]) {
-      const size_t hb = (static_cast<size_t>(wi.b) * H + wi.h) * N;
+  // to the stage by one warp (narrow layout: warp 2; wide causal: warp 2, the
+  // acc2 issuer, one block ahead of its accumulations; wide non-causal: warp 3).  A cursor walks this
+  // CTA's blocks; each step reads its block's L and D (two independent
+  // loads, in flight while the warp waits for the stage) and writes them.  A
+  // block's vectors sit in their own part of the stage (which TMA does not
+  // write) and go in as soon as the stage's previous round has been released.
+  constexpr int kU = kBlk / 32;
+  int v_it = -1, v_li = 0, v_t = 0, v_c = 0;
+  Item v_w{};
+  auto vec_begin = [&]() {
+    v_it = item_index(0, num_items);
+    if (v_it >= 0) v_w = decode_item<kDkDv, kCausal, kBlk>(v_it, N, H);
+  };
+  // write the cursor's block and advance; false if a wait gave up
+  auto vec_step = [&]() -> bool {
+    if (v_it < 0) return true;
+    float L[kU], Dv[kU];
+    const size_t hb = (static_cast<size_t>(v_w.b) * H + v_w.h) * N;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int q = (wi.i0 + ti) * kBlk + u * 32 + lane;
-        L[u] = -INFINITY;   // padded query: P = 0
-        Dv[u] = 0.0f;
-        if (q < N) {
-          L[u] = p.lse[hb + q];
-          Dv[u] = p.D[hb + q];
-        }
-      }
-    };
-    int it = item_index(0, num_items);
-    Item w{};
-    int t = 0;
-    float cl[U], cd[U];
-    if (it >= 0) {
-      w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
-      load(w, 0, cl, cd);
-    }
-    while (it >= 0) {
-      // the next block (possibly the next item's first)
-      Item wn = w;
-      int tn = t + 1, itn = it, lin = li;
-      if (tn >= w.nb) {
-        lin = li + 1;
-        itn = item_index(lin, num_items);
-        tn = 0;
-        if (itn >= 0) wn = decode_item<kDkDv, kCausal, kBlk>(itn, N, H);
-      }
-      float nl[U], nd[U];
-      if (itn >= 0) load(wn, tn, nl, nd);
-      const int s = c % S, round = c / S;
-      if (round > 0 &&
-          !warp_wait(&bars->c_empty[s], (round - 1) & 1, abort_flag, kWaitBudget)) {
-        ok = false;
-        break;
-      }
-      float* vec = stage_vec(s);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        // a fully masked query (L = -inf) gets P = 0 and dS = 0
-        const bool live = cl[u] != -INFINITY;
-        vec[u * 32 + lane] = live ? -cl[u] * kLog2e : -INFINITY;   // -L2: exponent s c + (-L2)
-        vec[kBlk + u * 32 + lane] = live ? -cd[u] : 0.0f;          // -D
-      }
-      mbar_arrive(&bars->vec_full[s]);
-      ++c;
-      w = wn;
-      t = tn;
-      it = itn;
-      li = lin;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        cl[u] = nl[u];
-        cd[u] = nd[u];
+    for (int u = 0; u < kU; ++u) {
+      const int q = (v_w.i0 + v_t) * kBlk + u * 32 + lane;
+      L[u] = -INFINITY;   // padded query: P = 0
+      Dv[u] = 0.0f;
+      if (q < N) {
+        L[u] = p.lse[hb + q];
+        Dv[u] = p.D[hb + q];
       }
     }
-    return ok;
+    const int s = v_c % S, round = v_c / S;
+    if (round > 0 &&
+        !warp_wait(&bars->c_empty[s], (round - 1) & 1, abort_flag, kWaitBudget))
+      return false;
+    float* vec = stage_vec(s);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      // a fully masked query (L = -inf) gets P = 0 and dS = 0
+      const bool live = L[u] != -INFINITY;
+      vec[u * 32 + lane] = live ? -L[u] * kLog2e : -INFINITY;   // -L2: exponent s c + (-L2)
+      vec[kBlk + u * 32 + lane] = live ? -Dv[u] : 0.0f;         // -D
+    }
+    mbar_arrive(&bars->vec_full[s]);
+    ++v_c;
+    if (++v_t >= v_w.nb) {
+      v_t = 0;
+      v_it = item_index(++v_li, num_items);
+      if (v_it >= 0) v_w = decode_item<kDkDv, kCausal, kBlk>(v_it, N, H);
+    }
+    return true;
   };
 
   // Role bodies; each runs inside the branch that sets its register budget
@@ -530,9 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_ss(tmem + Cfg::kTdP + col, dR2 + rbo + ro, dC2 + so + co, kIdescSP, kk > 0);
       };
       if (leader) {
-        // d = DP in the three-issuer kernel: fully unrolled with constant
-        // offsets (short issue stream); elsewhere the unrolled form costs
-        // spills in the issuing warp, so the loop stays
+        // d = DP in the three-issuer kernels: fully unrolled with constant
+        // offsets (short issue stream); elsewhere the loop, with descriptors
+        // advanced in place
         if (kThree && nks == DP / 16) {
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) step(kk);
@@ -608,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < w.nb; ++t) {
           const int cb = c + t;
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
-              !wait_acc_inputs(cb, t == 0, li)) {
+              !wait_acc_inputs(cb, t == 0, li, !kDkDv)) {
             ok = false;
             break;
           }
@@ -625,9 +605,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // second MMA warp (wide layout): the acc2 accumulations of every
         // block, concurrently with the acc1 ones (warp 3 with kThree, else
         // warp 1; a single issuing thread cannot keep the tensor pipe busy
-        // with N = 64 MMAs)
+        // with N = 64 MMAs).  In the dK/dV kernel it first writes the next
+        // block's per-query vectors (the first block's before the loop).
+        if (kDkDv && kThree && li == 0) {
+          vec_begin();
+          if (!vec_step()) {
+            ok = false;
+            break;
+          }
+        }
         for (int t = 0; t < w.nb; ++t) {
           const int cb = c + t;
+          if (kDkDv && kThree && !vec_step()) {
+            ok = false;
+            break;
+          }
           if (!warp_wait(&bars->pd_full, npd & 1, abort_flag, kWaitBudget) ||
               !wait_acc_inputs(cb, t == 0, li)) {
             ok = false;
@@ -715,18 +707,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (run && warp == 2) {
     // ===== narrow layout: per-query L and D of each streamed block (dK/dV) =====
-    if (kDkDv && !vec_loader() && lane == 0) raise_abort(bars, p.status);
+    if (kDkDv) {
+      bool ok = true;
+      vec_begin();
+      while (ok && v_it >= 0) ok = vec_step();
+      if (!ok && lane == 0) raise_abort(bars, p.status);
+    }
     __syncwarp();
   } else if (run && warp == 3) {
-    // ============ fp16 copy of each streamed C1 tile (same swizzled layout) ============
-    // Narrow layout: the whole copy.  Wide layout: no copy (the element-wise
-    // warps make it); in the dK/dV kernel the per-query -L2 and -D of each
-    // block; in the dQ kernel nothing (with kThree this warp is the third
-    // MMA issuer, above).
+    // ============ narrow layout: fp16 copy of each streamed C1 tile ============
+    // (same swizzled layout).  Wide layout: the element-wise warps make the
+    // copy, and this warp is the third MMA issuer, or (non-causal dK/dV
+    // kernel) writes the per-query vectors.
     int c = 0, li = 0;
     bool ok = true;
     if constexpr (kWide && kDkDv) {
-      ok = vec_loader();
+      vec_begin();
+      while (ok && v_it >= 0) ok = vec_step();
     } else if constexpr (!kWide) {
       for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
         const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
