@@ -16,16 +16,18 @@
 // contracted over their rows: Q^T and dO^T (for dK and dV), K^T (for dQ), as
 // [B, H, d, Np].
 //
-// One CTA per (b, h, 128-row tile), 6 warps:
+// One CTA per (b, h, 128-row tile), 8 warps:
 //   warp 0 lane 0   TMA: the resident row tiles R1, R2 (hi, lo) once; per
 //                   32-row streamed block, ring A (C1, C2 hi / lo: the
 //                   operands of S and dP, freed when those MMAs complete) and
 //                   ring B (the transposed operands of the accumulations,
 //                   freed when they complete);
-//   warp 1 lane 0   MMAs: S = R1 C1^T and dP = R2 C2^T (24 + 24 MMAs,
-//                   M = 128, N = 32, fp32 in TMEM), then the accumulations
-//                   from the hi / lo element-wise results in TMEM (12 MMAs
-//                   each, N = 64);
+//   warps 1, 7      MMAs (lane 0): S = R1 C1^T (warp 1) and dP = R2 C2^T
+//                   (warp 7), 24 MMAs each, M = 128, N = 32, fp32 in TMEM;
+//   warp 6 lane 0   MMAs: the accumulations from the hi / lo element-wise
+//                   results in TMEM (12 MMAs each, N = 64); three issuing
+//                   threads, since one thread's issue rate bounds these
+//                   N = 32 / 64 MMA streams;
 //   warps 2-5       one thread per owned row (TMEM lane): P = 2^(S c - L2),
 //                   dS = P (dP - D), masks, hi / lo split into TMEM; finally
 //                   the accumulators, scaled, as float32 rows.
@@ -56,7 +58,7 @@ namespace {
 constexpr int kRows = 128;               // rows owned by a CTA
 constexpr int kBlk = 32;                 // rows of a streamed block
 constexpr int kDP = 64;                  // padded head dim (d <= 64)
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
 constexpr int kRChunk = kRows * 128;     // 32 fp32 columns of 128 rows (16 KB)
 constexpr int kRTile = 2 * kRChunk;      // 128 x 64 fp32 (32 KB)
 constexpr int kCChunk = kBlk * 128;      // 32 fp32 columns of 32 rows (4 KB)
@@ -145,17 +147,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->r_full, 1);
     mbar_init(&bars->a_full, 1);
-    mbar_init(&bars->a_empty, 1);
+    mbar_init(&bars->a_empty, 2);   // S and dP issuers
     for (int s = 0; s < kBSlots; ++s) {
       mbar_init(&bars->b_full[s], 1);
       mbar_init(&bars->b_empty[s], 1);
     }
-    mbar_init(&bars->sp_full, 1);
+    mbar_init(&bars->sp_full, 2);   // S and dP issuers
     mbar_init(&bars->sp_free, kRows);
     mbar_init(&bars->x_full, kRows);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 3);   // one commit per MMA warp
     mbar_init(&bars->probe, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -225,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   }
-  else if (run && warp == 1) {
-    // ============== MMA issuer (whole warp waits, lane 0 issues) ==============
+  else if (run && (warp == 1 || warp == 6 || warp == 7)) {
+    // ====== MMA issuers (whole warp waits, lane 0 issues): warp 1 S, warp 7 dP, warp 6 the accumulations ======
     const bool leader = lane == 0;
     constexpr uint32_t kIdescSP = idesc_tf32(kRows, kBlk);   // S, dP: N = 32 streamed rows
     constexpr uint32_t kIdescAcc = idesc_tf32(kRows, kDP);   // accumulations: N = 64 columns
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            mbar_wait(&bars->sp_free, (i - 1) & 1, abort_flag, kWaitBudget))))
         return false;
       tc_fence_after();
-      if (leader) {
+      if (leader && warp == 1) {
 #pragma unroll
         for (int kk = 0; kk < kDP / 8; ++kk)
           mma_ss_tf32(tmem + kColS, dR1h + ks(kk, kRChunk), dC1h + ks(kk, kCChunk), kIdescSP,
@@ -259,6 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kDP / 8; ++kk)
           mma_ss_tf32(tmem + kColS, dR1l + ks(kk, kRChunk), dC1h + ks(kk, kCChunk), kIdescSP, 1u);
+      }
+      if (leader && warp == 7) {
 #pragma unroll
         for (int kk = 0; kk < kDP / 8; ++kk)
           mma_ss_tf32(tmem + kColdP, dR2h + ks(kk, kRChunk), dC2h + ks(kk, kCChunk), kIdescSP,
@@ -269,6 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kDP / 8; ++kk)
           mma_ss_tf32(tmem + kColdP, dR2l + ks(kk, kRChunk), dC2h + ks(kk, kCChunk), kIdescSP, 1u);
+      }
+      if (leader) {
         mma_commit(&bars->sp_full);
         mma_commit(&bars->a_empty);
       }
@@ -317,10 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    if (ok && nb > 0) ok = issue_sp(0);
-    for (int i = 0; i < nb && ok; ++i) {
-      if (i + 1 < nb && !issue_sp(i + 1)) ok = false;
-      if (ok && !issue_acc(i)) ok = false;
+    if (warp != 6) {
+      for (int i = 0; i < nb && ok; ++i)
+        if (!issue_sp(i)) ok = false;
+    } else {
+      for (int i = 0; i < nb && ok; ++i)
+        if (!issue_acc(i)) ok = false;
     }
     if (!ok && leader) bt_abort(bars, p.status);
     // no MMA may be in flight when TMEM is released
@@ -328,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(&bars->drain, 0, nullptr, kDrainBudget);
     __syncwarp();
   }
-  else if (run && warp >= 2) {
+  else if (run && warp >= 2 && warp <= 5) {
     // ============ element-wise warps 2-5: one thread per owned row ============
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
