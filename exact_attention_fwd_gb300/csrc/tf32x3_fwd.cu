@@ -17,13 +17,13 @@
 //      accesses) and V^T split as [B, H, d, Np] (Np = N rounded up to 4, zeros
 //      beyond N; transposed through shared-memory tiles), so that every MMA
 //      operand is K-major;
-//   2. fused pass, one CTA per (b, h, 128-row Q tile), 7 warps:
+//   2. fused pass, one CTA per (b, h, 128-row Q tile), 8 warps:
 //        warp 0 lane 0   TMA: Qh, Ql once; Kh, Kl of each key block into a
 //                        ring that S frees;
 //        warp 6 lane 0   TMA: V^Th, V^Tl of each block into a ring that P V
 //                        frees (the K loads run ahead of the V releases);
-//        warp 1 lane 0   MMAs: S = Qh Kh^T + Qh Kl^T + Ql Kh^T (fp32 in TMEM),
-//                        O += Ph Vh + Ph Vl + Pl Vh (P read from TMEM);
+//        warp 1 lane 0   MMAs: S = Qh Kh^T + Qh Kl^T + Ql Kh^T (fp32 in TMEM);
+//        warp 7 lane 0   MMAs: O += Ph Vh + Ph Vl + Pl Vh (P read from TMEM);
 //        warps 2-5       one thread per query row (TMEM lane): masked row max,
 //                        lazy rescale, P = 2^(s c - m) in float32 split into
 //                        Ph, Pl in TMEM; finally O / l and L.
@@ -49,7 +49,7 @@ namespace fa {
 namespace {
 
 constexpr int kBM = 128;                  // query rows per CTA
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;
 constexpr int kQChunk = kBM * 128;        // 32 fp32 columns of 128 rows
 constexpr int kTmemCols = 256;
 constexpr float kRescaleThreshold = 8.0f;
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->s_free, kBM);
     mbar_init(&bars->p_full, kBM);
     mbar_init(&bars->pv_done, 1);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);   // one commit per MMA warp
     mbar_init(&bars->probe, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -210,8 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   }
-  else if (run && warp == 1) {
-    // ================ MMA issuer (whole warp waits, lane 0 issues) ================
+  else if (run && (warp == 1 || warp == 7)) {
+    // ===== MMA issuers (whole warp waits, lane 0 issues): warp 1 S, warp 7 P V =====
+    // (one thread's issue rate bounds these N = 64 tf32 MMA streams, so the
+    // two chains come from separate threads)
     const bool leader = lane == 0;
     constexpr uint32_t kIdescS = idesc_tf32(kBM, kBN);   // S: N = kBN keys
     constexpr uint32_t kIdescPV = idesc_tf32(kBM, kDP);  // PV: N = DP columns
@@ -250,7 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    for (int j = 0; j < nb && ok; ++j) {
+    if (warp == 7) {
+      for (int jj = 0; jj < nb && ok; ++jj)
+        if (!pv_step(jj)) ok = false;
+    }
+    for (int j = 0; j < nb && ok && warp == 1; ++j) {
       const int s = j % kKStages;
       if (!__all_sync(0xffffffffu,
                       mbar_wait(&bars->k_full[s], (j / kKStages) & 1, abort_flag, kWaitBudget) &&
@@ -278,9 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars->k_empty[s]);
       }
       __syncwarp();
-      if (j > 0 && !pv_step(j - 1)) ok = false;
     }
-    if (ok && !pv_step(nb - 1)) ok = false;
     if (!ok && leader) tf32_abort(bars, p.status);
     // no MMA may be in flight when TMEM is released
     mma_commit_w(&bars->drain, leader ? 1u : 0u);
