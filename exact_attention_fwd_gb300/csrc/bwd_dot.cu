@@ -9,8 +9,10 @@
 // instruction of the warp is one contiguous 512-byte span.  When a row is a
 // power-of-two number of chunks (d = 8, 16, 32, 64, 128), each row belongs to
 // a fixed group of lanes, the row's partial dot products are summed with warp
-// shuffles, and every lane keeps 4 rows' chunks of both tensors in flight;
-// other head sizes stage the partial sums in shared memory.
+// shuffles, and every lane keeps 2 rows' chunks of both tensors in flight (more
+// raised the register count and lowered the resident warps: measured slower);
+// other head sizes stage the partial sums in shared memory.  The grid is the
+// number of blocks that fit on the SMs at once, each striding over the rows.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) dot_do_o_kernel(BwdParams p) {
 template <int kElt, int kCpr>
 __global__ void __launch_bounds__(kThreads) dot_shfl_kernel(BwdParams p) {
   constexpr int kRowsPass = 32 / kCpr;
-  constexpr int kUnroll = 4;
+  constexpr int kUnroll = 2;
   constexpr int kRowsIter = kRowsPass * kUnroll;
   const int lane = threadIdx.x & 31, sub = lane % kCpr, rr = lane / kCpr;
   const long long rows = static_cast<long long>(p.B) * p.N * p.H;
@@ -132,11 +134,19 @@ __global__ void __launch_bounds__(kThreads) dot_shfl_kernel(BwdParams p) {
       const long long r = r0 + u * kRowsPass + rr;
       if (sub == 0 && r < rows) {
         // flattened row r = (b * N + n) * H + h  ->  D[(b * H + h) * N + n]
-        const int h = static_cast<int>(r % p.H);
-        const long long bn = r / p.H;
-        const int n = static_cast<int>(bn % p.N);
-        const long long bb = bn / p.N;
-        p.D[(bb * p.H + h) * p.N + n] = s;
+        // (32-bit division where the row count allows: fewer registers)
+        if (rows <= 0x7fffffffLL) {
+          const unsigned ru = static_cast<unsigned>(r), Hu = static_cast<unsigned>(p.H),
+                         Nu = static_cast<unsigned>(p.N);
+          const unsigned h = ru % Hu, bn = ru / Hu, n = bn % Nu, bb = bn / Nu;
+          p.D[(static_cast<size_t>(bb) * Hu + h) * Nu + n] = s;
+        } else {
+          const int h = static_cast<int>(r % p.H);
+          const long long bn = r / p.H;
+          const int n = static_cast<int>(bn % p.N);
+          const long long bb = bn / p.N;
+          p.D[(bb * p.H + h) * p.N + n] = s;
+        }
       }
     }
   }
@@ -164,14 +174,19 @@ cudaError_t launch_bwd_dot(const BwdParams& p, int elt, cudaStream_t s) {
   const long long rows = static_cast<long long>(p.B) * p.N * p.H;
   const long long groups = (rows + kRowsPerWarp - 1) / kRowsPerWarp;
   long long blocks = (groups + (kThreads / 32) - 1) / (kThreads / 32);
-  const long long cap = static_cast<long long>(sms > 0 ? sms : 148) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
   void* args[] = {const_cast<BwdParams*>(&p)};
   const int cpr = p.d * (elt == 0 ? 4 : 2) / 16;   // 16-byte chunks per row
   const void* kern = elt == 2   ? dot_kernel_for<2>(cpr)
                      : elt == 1 ? dot_kernel_for<1>(cpr)
                                 : dot_kernel_for<0>(cpr);
+  // as many blocks as are resident at once (each strides over the rows)
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const long long cap = static_cast<long long>(sms > 0 ? sms : 148) * per_sm;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
   return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), args, 0, s);
 }
 
