@@ -77,22 +77,26 @@ constexpr int kRegsElem = 208;     // warps 4-11: element-wise and epilogue
 static_assert(4 * 32 * kRegsHelper + 8 * 32 * kRegsElem <= 168 * kThreads,
               "register split exceeds the launch allocation");
 constexpr int kTmemCols = 512;
-constexpr int kStagesMax = 3;
+constexpr int kStagesMax = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int DP>
 struct BwdCfg {
   static constexpr bool kWide = (DP == 64);
   static constexpr int kBlk = kWide ? 128 : 64;          // rows of one streamed block
-  static constexpr int kStages = 3;
+  // wide layout: the fp16 copy of C1 overwrites the bf16 tile in place (made
+  // once the block's S has been computed, its only bf16 reader), so a stage
+  // is two tiles and four stages fit; narrow: a separate copy, three stages
+  static constexpr int kStages = kWide ? 4 : 3;
   static constexpr int kChunks = DP / 64;
   static constexpr int kRowChunk = kRows * 128;          // 16 KB: 128 rows x 64 cols
   static constexpr int kBlkChunk = kBlk * 128;           // rows x 64 cols
   static constexpr int kRowTile = kChunks * kRowChunk;
   static constexpr int kBlkTile = kChunks * kBlkChunk;
   static constexpr int kVecBytes = 1024;                 // L2 and D of up to 128 queries
-  // stage: C1 (bf16) | C2 (bf16) | C1 as fp16 | vectors
-  static constexpr int kStageBytes = 3 * kBlkTile + kVecBytes;
+  // stage: C1 (bf16, then fp16 in the wide layout) | C2 (bf16) | [narrow: C1 as fp16] | vectors
+  static constexpr int kStageTiles = kWide ? 2 : 3;
+  static constexpr int kStageBytes = kStageTiles * kBlkTile + kVecBytes;
   static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
   // row tiles (R1, R2) of an item; the wide layout double-buffers them so
   // the next item's rows load while this item's last blocks run
@@ -350,12 +354,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sR2 = smem + Cfg::kR2Off;
   auto stage_c1 = [&](int s) { return smem + Cfg::kStageOff + s * Cfg::kStageBytes; };
   auto stage_c2 = [&](int s) { return stage_c1(s) + Cfg::kBlkTile; };
-  auto stage_c1h = [&](int s) { return stage_c1(s) + 2 * Cfg::kBlkTile; };
+  auto stage_c1h = [&](int s) { return Cfg::kWide ? stage_c1(s) : stage_c1(s) + 2 * Cfg::kBlkTile; };
   auto stage_vec = [&](int s) {
-    return reinterpret_cast<float*>(stage_c1(s) + 3 * Cfg::kBlkTile);
+    return reinterpret_cast<float*>(stage_c1(s) + Cfg::kStageTiles * Cfg::kBlkTile);
   };
 
-  // fp16 copy of part [v0, v1) (16-byte units) of stage s's C1 tile, same
+  // fp16 copy of part [v0, v1) (16-byte units) of stage s's C1 tile (in place in the
+  // wide layout, once the block's S has been computed), same
   // swizzled layout; the lanes of one warp share the range
   // (threads: tid = 0 .. nthr-1 share the range)
   auto convert_c1 = [&](int s, int v0, int v1, int tid, int nthr) {
