@@ -19,7 +19,7 @@ EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_phase", "fa_bwd_workspace_size", "fa_sync
            "fa_fwd_splitkv_keys_per_split", "fa_fwd_splitkv_workspace_size", "fa_fwd_splitkv",
            "fa_fwd_bwd_host_workspace_size", "fa_fwd_bwd_host", "fa_fwd_unfused_workspace_size",
            "fa_fwd_unfused", "fa_fwd_tf32x3_workspace_size", "fa_fwd_tf32x3",
-           "fa_bwd_tf32x3_workspace_size", "fa_bwd_tf32x3")
+           "fa_bwd_tf32x3_workspace_size", "fa_bwd_tf32x3", "fa_bwd_prepass")
 FA_BWD_NOALLOC_MAX_ROWS = 1 << 22
 
 _lib = None
@@ -80,6 +80,8 @@ def load():
     lib.fa_bwd_tf32x3_workspace_size.restype = sz
     lib.fa_bwd_tf32x3.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_bwd_tf32x3.restype = i
+    lib.fa_bwd_prepass.argtypes = [i, i]
+    lib.fa_bwd_prepass.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -114,6 +116,11 @@ def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, d
     """fa_bwd with the library's fixed device scratch instead of a workspace."""
     return load().fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, float(scale),
                                  int(causal), int(dtype), int(grad_dtype), stream)
+
+
+def fa_bwd_prepass(d, dtype):
+    """1 if fa_bwd's phase 0 launches the D pre-pass for this d and dtype."""
+    return int(load().fa_bwd_prepass(int(d), int(dtype)))
 
 
 def fa_bwd_workspace_size(B, H, N):

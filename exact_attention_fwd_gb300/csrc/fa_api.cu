@@ -180,10 +180,15 @@ fa_status prepare_bwd(const void* q, const void* k, const void* v, const void* o
   return FA_OK;
 }
 
+// 16-bit inputs with d <= 64: the dQ kernel forms D's first estimate from the
+// O and dO rows it loads, so phase 0 launches nothing
+bool bwd_prepass(int d, fa_dtype dtype) { return dtype == FA_DTYPE_F32 || d > 64; }
+
 fa_status run_bwd_phase(const fa::BwdParams& p, int phase, fa_dtype dtype, bool causal,
                         cudaStream_t s) {
   cudaError_t e;
   if (phase == 0) {
+    if (!bwd_prepass(p.d, dtype)) return FA_OK;
     e = fa::launch_bwd_dot(p, dtype == FA_DTYPE_F32 ? 0 : (dtype == FA_DTYPE_BF16 ? 1 : 2), s);
   } else if (dtype == FA_DTYPE_F32) {
     e = fa::launch_bwd_simt_f32(p, s, causal, phase);
@@ -211,6 +216,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     st = run_bwd_phase(p, phase, dtype, causal != 0, s);
   return st;
 }
+
+int fa_bwd_prepass(int d, fa_dtype dtype) { return bwd_prepass(d, dtype) ? 1 : 0; }
 
 fa_status fa_bwd_phase(int phase, const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,

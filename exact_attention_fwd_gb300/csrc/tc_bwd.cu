@@ -80,14 +80,19 @@ constexpr int kTmemCols = 512;
 constexpr int kStagesMax = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int DP>
+template <int DP, bool kDkDv>
 struct BwdCfg {
   static constexpr bool kWide = (DP == 64);
+  // the wide dQ kernel also loads each item's O rows (third row tile): it
+  // forms the first estimate of D = rowsum(dO * O) itself, so that path has
+  // no D pre-pass
+  static constexpr bool kOwnD = kWide && !kDkDv;
+  static constexpr int kRTiles = kOwnD ? 3 : 2;
   static constexpr int kBlk = kWide ? 128 : 64;          // rows of one streamed block
   // wide layout: the fp16 copy of C1 overwrites the bf16 tile in place (made
   // once the block's S has been computed, its only bf16 reader), so a stage
   // is two tiles and four stages fit; narrow: a separate copy, three stages
-  static constexpr int kStages = kWide ? 4 : 3;
+  static constexpr int kStages = (kWide && kDkDv) ? 4 : 3;
   static constexpr int kChunks = DP / 64;
   static constexpr int kRowChunk = kRows * 128;          // 16 KB: 128 rows x 64 cols
   static constexpr int kBlkChunk = kBlk * 128;           // rows x 64 cols
@@ -103,11 +108,13 @@ struct BwdCfg {
   static constexpr int kRBufs = kWide ? 2 : 1;
   static constexpr int kR1Off = 0;
   static constexpr int kR2Off = kRowTile;
-  static constexpr int kRBufBytes = 2 * kRowTile;
+  static constexpr int kR3Off = 2 * kRowTile;               // O rows (kOwnD)
+  static constexpr int kRBufBytes = kRTiles * kRowTile;
   static constexpr int kStageOff = kRBufs * kRBufBytes;
   static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
   static constexpr int kDsumOff = kBarOff + 512;         // 2 items x 2 warpgroups x 128
-  static constexpr int kSmemBytes = kDsumOff + 2048 + 1024;
+  static constexpr int kDpartOff = kDsumOff + 2048;      // the same, for D's estimate (kOwnD)
+  static constexpr int kSmemBytes = kDpartOff + 2048 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory per block");
   // TMEM columns
   static constexpr int kTS = 0;
@@ -125,7 +132,7 @@ struct BwdBars {
   uint64_t vec_full[kStagesMax], conv_full[kStagesMax];
   uint64_t sp_full, sp_free, pd_full, acc_done;   // wide layout
   uint64_t s_full[2], p_full[2];                  // narrow layout
-  uint64_t acc_full, acc_free, dsum;
+  uint64_t acc_full, acc_free, dsum, dpart;
   uint64_t epi_staged;   // wide layout, bf16 gradients: the staging tiles are written
   uint64_t drain, probe;
   uint32_t tmem_base;
@@ -281,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
                   const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmC2,
                   const __grid_constant__ CUtensorMap tmG1, const __grid_constant__ CUtensorMap tmG2,
-                  const BwdParams p) {
-  using Cfg = BwdCfg<DP>;
+                  const __grid_constant__ CUtensorMap tmR3, const BwdParams p) {
+  using Cfg = BwdCfg<DP, kDkDv>;
   // S/dP, acc1 and acc2 from three issuing warps (1, 3, 2): the wide dQ
   // kernels and the causal wide dK/dV kernel (the fp16 copies are made by the
   // element-wise warps; in that dK/dV kernel warp 2 also writes the
@@ -297,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + Cfg::kBarOff);
   float* dsum = reinterpret_cast<float*>(smem + Cfg::kDsumOff);
+  float* dpart = reinterpret_cast<float*>(smem + Cfg::kDpartOff);
   const volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int N = p.N, H = p.H;
@@ -327,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->acc_full, kWide ? 2 : 1);
     mbar_init(&bars->acc_free, 256);
     mbar_init(&bars->dsum, 256);
+    mbar_init(&bars->dpart, 256);
     mbar_init(&bars->epi_staged, 256);
     mbar_init(&bars->drain, kThree ? 3 : (kWide ? 2 : 1));   // one commit per MMA warp
     mbar_init(&bars->probe, 1);
@@ -453,12 +462,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* r1 = sR1 + rb * Cfg::kRBufBytes;
         uint8_t* r2 = sR2 + rb * Cfg::kRBufBytes;
-        mbar_arrive_expect_tx(&bars->r_full[rb], 2 * Cfg::kRowTile);
+        mbar_arrive_expect_tx(&bars->r_full[rb], Cfg::kRTiles * Cfg::kRowTile);
         for (int ch = 0; ch < Cfg::kChunks; ++ch) {
           tma_load_4d(r1 + ch * Cfg::kRowChunk, &tmR1, &bars->r_full[rb], ch * 64, w.h, w.row0,
                       w.b);
           tma_load_4d(r2 + ch * Cfg::kRowChunk, &tmR2, &bars->r_full[rb], ch * 64, w.h, w.row0,
                       w.b);
+          if constexpr (Cfg::kOwnD)
+            tma_load_4d(sR1 + rb * Cfg::kRBufBytes + Cfg::kR3Off + ch * Cfg::kRowChunk, &tmR3,
+                        &bars->r_full[rb], ch * 64, w.h, w.row0, w.b);
         }
         ++li;
         for (int t = 0; t < w.nb; ++t) {
@@ -787,11 +799,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (g2 < N) {
         const size_t hb2 = (static_cast<size_t>(w2.b) * H + w2.h) * N;
         L = p.lse[hb2 + g2];
-        Dv = p.D[hb2 + g2];
+        if (!Cfg::kOwnD) Dv = p.D[hb2 + g2];
       }
     };
     float L_nx = -INFINITY, D_nx = 0.0f;
     if (!kDkDv) load_row(item_index(0, num_items), L_nx, D_nx);
+    // wide dQ kernel: D's first estimate, the float32 dot of this query's dO
+    // and O rows (bf16 or fp16, in the item's row buffer, 128-byte swizzle);
+    // warpgroup g takes 16-byte chunks [4g, 4g + 4) of the row
+    auto row_dot = [&](int rb) -> float {
+      const uint8_t* rdo = sR2 + rb * Cfg::kRBufBytes + row * 128;
+      const uint8_t* ro = sR1 + rb * Cfg::kRBufBytes + Cfg::kR3Off + row * 128;
+      uint64_t acc[4] = {0, 0, 0, 0};   // four packed f32x2 chains (+0.0f pairs)
+#pragma unroll
+      for (int cq = 0; cq < 4; ++cq) {
+        const int ck = 4 * g + cq;
+        const int off = (ck ^ (row & 7)) << 4;
+        const uint4 a = *reinterpret_cast<const uint4*>(rdo + off);
+        const uint4 b = *reinterpret_cast<const uint4*>(ro + off);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float2 x, y;
+          if constexpr (kF16) {
+            x = __half22float2(*reinterpret_cast<const __half2*>(&av[i]));
+            y = __half22float2(*reinterpret_cast<const __half2*>(&bv[i]));
+          } else {
+            x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[i]));
+            y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[i]));
+          }
+          acc[i] = f2_fma(f2_pack(x.x, x.y), f2_pack(y.x, y.y), acc[i]);
+        }
+      }
+      const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+      return f2_lo(s2) + f2_hi(s2);
+    };
     for (int it = item_index(0, num_items); it >= 0 && ok; it = item_index(++li, num_items)) {
       const Item w = decode_item<kDkDv, kCausal, kBlk>(it, N, H);
       const int grow = w.row0 + row;      // query (dQ) or key (dK/dV)
@@ -799,8 +841,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l2_row = INFINITY, d_row = 0.0f;          // dQ kernel: this query's L, D~
       bool live_row = false;
       if (!kDkDv) {
-        const float L = L_nx, Dv = D_nx;
+        const float L = L_nx;
+        float Dv = D_nx;
         load_row(item_index(li + 1, num_items), L_nx, D_nx);
+        if constexpr (Cfg::kOwnD) {
+          // the item's rows have landed (also what the MMA warp waits for)
+          const int rb = li % Cfg::kRBufs;
+          if (!warp_wait(&bars->r_full[rb], (li / Cfg::kRBufs) & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
+          }
+          // the two warpgroups' halves of the dot, exchanged through shared
+          // memory (each item's slot pair alternates)
+          float* dp = dpart + (li & 1) * 256;
+          dp[g * kRows + row] = row_dot(rb);
+          mbar_arrive(&bars->dpart);
+          if (!warp_wait(&bars->dpart, li & 1, abort_flag, kWaitBudget)) {
+            ok = false;
+            break;
+          }
+          Dv = dp[row] + dp[kRows + row];
+        }
         if (grow < N && L != -INFINITY) {
           live_row = true;
           l2_row = L * kLog2e;
@@ -1041,7 +1102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(&bars->dsum, li & 1, abort_flag, kWaitBudget)) { ok = false; break; }
         const float d_exact = ds_item[row] + ds_item[kRows + row];
         corr = d_row - d_exact;
-        if (g == 0 && live_row) p.D[hb + grow] = d_exact;
+        if (g == 0 && grow < N) p.D[hb + grow] = live_row ? d_exact : 0.0f;
       }
       if (!warp_wait(&bars->acc_full, li & 1, abort_flag, kWaitBudget)) { ok = false; break; }
       tc_fence_after();
@@ -1142,8 +1203,8 @@ int sm_count() {
 
 template <int DP, bool kCausal, bool kDkDv, bool kF32, bool kF16>
 cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
-  using Cfg = BwdCfg<DP>;
-  CUtensorMap m[6];
+  using Cfg = BwdCfg<DP, kDkDv>;
+  CUtensorMap m[7];
   // dQ:    rows are Q, dO (128-row boxes), blocks are K, V.
   // dK/dV: rows are K, V, blocks are Q, dO.
   const void* r1 = kDkDv ? p.k : p.q;
@@ -1163,6 +1224,10 @@ cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
     if (e == cudaSuccess && kDkDv)
       e = make_bhnd_tmap(&m[5], p.dk, p.B, p.N, p.H, p.d, kRows, 64, kF16);
   }
+  // the wide dQ kernel's O rows (it forms D's first estimate itself)
+  m[6] = m[0];
+  if (e == cudaSuccess && Cfg::kOwnD)
+    e = make_bhnd_tmap(&m[6], p.o, p.B, p.N, p.H, p.d, kRows, 64, kF16);
   if (e != cudaSuccess) return e;
   auto kern = bwd_tc_kernel<DP, kCausal, kDkDv, kF32, kF16>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
@@ -1173,7 +1238,7 @@ cudaError_t launch_one(const BwdParams& p, cudaStream_t st) {
   if (sms <= 0) return cudaErrorInvalidDevice;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   BwdParams pc = p;
-  void* args[] = {&m[0], &m[1], &m[2], &m[3], &m[4], &m[5], &pc};
+  void* args[] = {&m[0], &m[1], &m[2], &m[3], &m[4], &m[5], &m[6], &pc};
   return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads), args,
                           Cfg::kSmemBytes, st);
 }

@@ -117,7 +117,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
  * on one stream, and the phases must be run in that order:
  *   0: the D pre-pass, D = rowsum(dO * O) into the workspace
  *      ("Flash Attention 2 — backward pass notes", option 1 of "Why the WGSL
- *      kernel isn't shipped this turn");
+ *      kernel isn't shipped this turn"); with 16-bit inputs and d <= 64 it
+ *      launches nothing, because phase 1 forms D from the O and dO rows it
+ *      loads;
  *   1: the kernel that owns Q tiles and writes dQ (16-bit paths: also
  *      refines D in the workspace);
  *   2: the kernel that owns K tiles and writes dK and dV (option 3).
@@ -130,6 +132,14 @@ fa_status fa_bwd_phase(int phase, const void* q, const void* k, const void* v, c
                        int B, int H, int N, int d, float scale, int causal,
                        fa_dtype dtype, fa_dtype grad_dtype,
                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_bwd_prepass — 1 if fa_bwd's phase 0 (the D pre-pass) launches a kernel
+ * for this head dim and input type, 0 if it is empty (16-bit inputs with
+ * d <= 64: phase 1 forms D itself); for callers that time the phases.  No
+ * argument checks: it only reports the rule.
+ */
+int fa_bwd_prepass(int d, fa_dtype dtype);
 
 /*
  * fa_sync_status — synchronises `stream`, then returns and clears the device

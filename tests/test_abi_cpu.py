@@ -53,6 +53,18 @@ def test_status_strings(lib):
     assert _lib.status_string(99) == "FA_ERR_UNKNOWN"
 
 
+def test_bwd_prepass_rule(lib):
+    """Phase 0 is empty exactly for 16-bit inputs with d <= 64."""
+    from exact_attention_fwd_gb300 import _lib
+    for d in (8, 64):
+        assert _lib.fa_bwd_prepass(d, _lib.FA_DTYPE_BF16) == 0
+        assert _lib.fa_bwd_prepass(d, _lib.FA_DTYPE_F16) == 0
+        assert _lib.fa_bwd_prepass(d, _lib.FA_DTYPE_F32) == 1
+    for d in (72, 128):
+        assert _lib.fa_bwd_prepass(d, _lib.FA_DTYPE_BF16) == 1
+        assert _lib.fa_bwd_prepass(d, _lib.FA_DTYPE_F32) == 1
+
+
 def test_workspace_size(lib):
     from exact_attention_fwd_gb300 import _lib
     assert _lib.fa_bwd_workspace_size(64, 16, 1024) == 64 * 16 * 1024 * 4
