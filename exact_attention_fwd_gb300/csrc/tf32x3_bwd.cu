@@ -529,7 +529,7 @@ cudaError_t launch_bwd_tf32x3(const BwdParams& p_in, void* workspace, cudaStream
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (static_cast<long long>(B) * H > 65535) return cudaErrorInvalidConfiguration;
-  const dim3 tgrid((Np + 31) / 32, (d + 31) / 32, B * H);
+  const dim3 tgrid((Np + 31) / 32, (d + 63) / 64, B * H);
   const float* tsrc[3] = {static_cast<const float*>(p.q), static_cast<const float*>(p.k),
                           static_cast<const float*>(p.dO)};
   for (int i = 0; i < 3; ++i)

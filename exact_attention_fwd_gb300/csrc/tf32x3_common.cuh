@@ -88,29 +88,41 @@ __global__ void __launch_bounds__(256) split_qk_kernel(const float4* q, const fl
   }
 }
 
-// Split pass, V: the transposed split V^T [B, H, d, Np] through 32 x 32 tiles
-// in shared memory, so reads (along d) and writes (along n) are both
-// contiguous.  Block (n-tile, c-tile, b * H + h) with 32 x 8 threads; columns
-// n in [N, Np) are written as zeros.
+// V^T split: [B, N, H, d] -> hi / lo as [B, H, d, Np] (Np = N rounded up to
+// 4; rows n >= N are written as zeros).  A CTA transposes 32 rows (n) by 64
+// columns (c) of one (b, h) through one shared-memory tile: 16-byte loads of
+// V rows, 16-byte stores of V^T rows, index arithmetic once per CTA.
 __global__ void __launch_bounds__(256) split_vt_kernel(const float* v, float* vth, float* vtl,
                                                        int N, int H, int d, int Np) {
-  __shared__ float tile[32][33];
-  const int n0 = blockIdx.x * 32, c0 = blockIdx.y * 32, bh = blockIdx.z;
+  __shared__ float tile[32][65];
+  const int n0 = blockIdx.x * 32, c0 = blockIdx.y * 64, bh = blockIdx.z;
   const int b = bh / H, h = bh % H;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  for (int r = ty; r < 32; r += 8) {
-    const int n = n0 + r, c = c0 + tx;
-    tile[r][tx] = (n < N && c < d) ? v[((static_cast<size_t>(b) * N + n) * H + h) * d + c] : 0.0f;
+  const size_t rs = static_cast<size_t>(H) * d;   // floats between V rows
+  const float* vb = v + (static_cast<size_t>(b) * N * H + h) * d;
+  for (int i = threadIdx.x; i < 32 * 16; i += 256) {
+    const int r = i >> 4, c4 = (i & 15) * 4, n = n0 + r, c = c0 + c4;
+    float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (n < N && c < d) x = *reinterpret_cast<const float4*>(vb + n * rs + c);
+    tile[r][c4] = x.x;
+    tile[r][c4 + 1] = x.y;
+    tile[r][c4 + 2] = x.z;
+    tile[r][c4 + 3] = x.w;
   }
   __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
-    const int c = c0 + r, n = n0 + tx;
-    if (c < d && n < Np) {
-      const float x = tile[tx][r];
-      const float xh = tf32_rn(x);
-      const size_t o = (static_cast<size_t>(bh) * d + c) * Np + n;
-      vth[o] = xh;
-      vtl[o] = tf32_rn(x - xh);
+  const size_t ob = (static_cast<size_t>(bh) * d + c0) * Np + n0;
+  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+    const int c = i >> 3, n4 = (i & 7) * 4;
+    if (c0 + c < d && n0 + n4 < Np) {
+      float xs[4], hs[4], ls[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xs[j] = tile[n4 + j][c];
+        hs[j] = tf32_rn(xs[j]);
+        ls[j] = tf32_rn(xs[j] - hs[j]);
+      }
+      const size_t o = ob + static_cast<size_t>(c) * Np + n4;
+      *reinterpret_cast<float4*>(vth + o) = make_float4(hs[0], hs[1], hs[2], hs[3]);
+      *reinterpret_cast<float4*>(vtl + o) = make_float4(ls[0], ls[1], ls[2], ls[3]);
     }
   }
 }

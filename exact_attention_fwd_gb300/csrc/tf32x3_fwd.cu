@@ -489,7 +489,7 @@ cudaError_t launch_t3(const FwdParams& p, void* workspace, cudaStream_t st, bool
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (static_cast<long long>(B) * H > 65535) return cudaErrorInvalidConfiguration;
-  split_vt_kernel<<<dim3((Np + 31) / 32, (d + 31) / 32, B * H), 256, 0, st>>>(
+  split_vt_kernel<<<dim3((Np + 31) / 32, (d + 63) / 64, B * H), 256, 0, st>>>(
       static_cast<const float*>(p.v), vth, vtl, N, H, d, Np);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
