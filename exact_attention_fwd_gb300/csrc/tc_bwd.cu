@@ -10,12 +10,14 @@
 // float atomics.  Rows whose L is -inf contribute nothing ("Caveats specific
 // to the backward path").
 //
-// Precision.  The forward stores O in bf16, and D computed from that O (the
-// pre-pass, bwd_dot.cu) is off by up to |dO| |O| 2^-9 per row; the gradient
-// amplifies that by |K| scale, which exceeds the bf16 gradient tolerance when
-// Q and K have large entries.  The dQ kernel therefore also accumulates the
-// exact-form D_i = sum_j P_ij dP_ij in fp32 and B_i = sum_j P_ij K_j, runs its
-// loop with the pre-pass value D~ and adds scale (D~_i - D_i) B_i at the end
+// Precision.  The forward stores O in bf16, and D computed from that O is off
+// by up to |dO| |O| 2^-9 per row; the gradient amplifies that by |K| scale,
+// which exceeds the bf16 gradient tolerance when Q and K have large entries.
+// The dQ kernel therefore also accumulates the exact-form D_i =
+// sum_j P_ij dP_ij in fp32 and B_i = sum_j P_ij K_j, runs its loop with the
+// estimate D~ from the bf16 O (formed by the dQ kernel itself from the O and
+// dO rows it loads in the wide layout, by the pre-pass bwd_dot.cu in the
+// narrow one) and adds scale (D~_i - D_i) B_i at the end
 // (algebraically the same dQ); it writes the refined D back to the workspace,
 // and the dK/dV kernel, launched after it, uses that.  dS (and P for B) are
 // staged for the tensor cores in fp16, whose 11-bit significand keeps the
@@ -26,7 +28,8 @@
 // Both kernels share one persistent skeleton (template parameter kDkDv): one
 // CTA per SM walks work items, each a 128-row tile of one (b, h):
 //   row tile   : resident in shared memory for the item.  dQ kernel: Q and dO
-//                of 128 queries.  dK/dV kernel: K and V of 128 keys.
+//                of 128 queries (and, wide layout, O for D's estimate).
+//                dK/dV kernel: K and V of 128 keys.
 //   blocks     : streamed through a TMA ring.  dQ: K_j, V_j.  dK/dV: Q_i, dO_i
 //                (plus their L and D).
 //   per block  : S = R1 C1^T and dP = R2 C2^T (tcgen05, M=128, bf16, both
@@ -51,11 +54,17 @@
 // streamed tiles through L2) and odd waves run in reverse CTA order, which
 // pairs long and short causal tiles on each CTA.
 //
-// Roles (12 warps): warp 0 TMA producer, warp 1 MMA issuer (converged, lane 0
-// issues), warp 2 loads the per-query L and D of each block (dK/dV kernel),
-// warp 3 converts each streamed C1 tile to fp16, warps 4-7 and 8-11 are the
-// element-wise warpgroups and the epilogue (each stores half of the columns
-// of the accumulator rows).
+// Roles (12 warps): warp 0 TMA producer; warp 1 issues the MMAs (converged,
+// lane 0 issues) — in the wide dQ kernels and the wide causal dK/dV kernel
+// only S/dP, with warp 3 issuing the first accumulation and warp 2 the second
+// (elsewhere warp 1 also issues the first and warp 2 the second); the
+// per-query -L2 and -D of each streamed block (dK/dV kernel) are written by
+// warp 2 (narrow layout, and one block ahead of its dK MMAs in the wide
+// causal kernel) or warp 3 (wide non-causal); the fp16 copy of each streamed
+// C1 tile is made by the element-wise warps in the wide layout (in place over
+// the bf16 tile, once the block's S has read it) and by warp 3 in the narrow
+// one; warps 4-7 and 8-11 are the element-wise warpgroups and the epilogue
+// (each stores half of the columns of the accumulator rows).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
