@@ -101,7 +101,11 @@ struct BwdCfg {
   // wide layout: the fp16 copy of C1 overwrites the bf16 tile in place (made
   // once the block's S has been computed, its only bf16 reader), so a stage
   // is two tiles and four stages fit; narrow: a separate copy, three stages
-  static constexpr int kStages = (kWide && kDkDv) ? 4 : 3;
+  static constexpr int kStages = 3;
+  // wide dK/dV kernel: an item's epilogue is deferred to the next item's first
+  // block, so its row buffer (where the gradient rows are staged) is held a
+  // little longer; a third buffer keeps the next-but-one item's rows loading
+  static constexpr bool kDefer = kWide && kDkDv;
   static constexpr int kChunks = DP / 64;
   static constexpr int kRowChunk = kRows * 128;          // 16 KB: 128 rows x 64 cols
   static constexpr int kBlkChunk = kBlk * 128;           // rows x 64 cols
@@ -114,7 +118,7 @@ struct BwdCfg {
   static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
   // row tiles (R1, R2) of an item; the wide layout double-buffers them so
   // the next item's rows load while this item's last blocks run
-  static constexpr int kRBufs = kWide ? 2 : 1;
+  static constexpr int kRBufs = kWide ? (kDefer ? 3 : 2) : 1;
   static constexpr int kR1Off = 0;
   static constexpr int kR2Off = kRowTile;
   static constexpr int kR3Off = 2 * kRowTile;               // O rows (kOwnD)
@@ -136,7 +140,7 @@ struct BwdCfg {
 };
 
 struct BwdBars {
-  uint64_t r_full[2], r_empty[2];
+  uint64_t r_full[3], r_empty[3];
   uint64_t c_full[kStagesMax], c_empty[kStagesMax];
   uint64_t vec_full[kStagesMax], conv_full[kStagesMax];
   uint64_t sp_full, sp_free, pd_full, acc_done;   // wide layout
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- setup ----
   if (threadIdx.x == 0) {
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
       mbar_init(&bars->r_full[b], 1);
       mbar_init(&bars->r_empty[b], 1);
     }
@@ -811,6 +815,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!Cfg::kOwnD) Dv = p.D[hb2 + g2];
       }
     };
+    // An item's epilogue: wait for its last accumulations, then this
+    // warpgroup stores half of the accumulator columns (dQ: with the
+    // correction corr of its D refinement).  The wide dK/dV kernel defers it
+    // to the next item's first block, after that block's element-wise math
+    // and before its P and dS overwrite the TMEM the accumulations read.
+    auto epilogue = [&](const Item& ew, int eli, float corr) -> bool {
+      if (!warp_wait(&bars->acc_full, eli & 1, abort_flag, kWaitBudget)) return false;
+      tc_fence_after();
+      const int egrow = ew.row0 + row;
+      const bool store = egrow < N;
+      const size_t roff = ((static_cast<size_t>(ew.b) * N + (store ? egrow : 0)) * H + ew.h) *
+                          static_cast<size_t>(p.d);
+      const int half_cols = DP / 2;
+      const int cbeg = g * half_cols;
+      auto row_ptr = [&](void* base) -> void* {
+        return kF32Grad ? static_cast<void*>(static_cast<float*>(base) + roff)
+                        : static_cast<void*>(static_cast<__nv_bfloat16*>(base) + roff);
+      };
+      if constexpr (kWide && !kF32Grad) {
+        // Wide layout, bf16 gradients: stage the rows in this item's row
+        // buffer (its last S/dP MMAs have completed, acc_full says so) and
+        // write them with TMA tensor stores; the buffer is released to the
+        // producer once the stores have read it.
+        const int rb = eli % Cfg::kRBufs;
+        uint8_t* st1 = sR1 + rb * Cfg::kRBufBytes;
+        uint8_t* st2 = sR2 + rb * Cfg::kRBufBytes;
+        if (kDkDv) {
+          stage_acc_cols<false, kF16>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg, half_cols, 1.0f,
+                                st1, row);
+          stage_acc_cols<false, kF16>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg, half_cols, p.scale,
+                                st2, row);
+        } else {
+          stage_acc_cols<true, kF16>(tmem + lane_base + Cfg::kTAcc2, tmem + lane_base + Cfg::kTAcc1, corr,
+                               cbeg, half_cols, p.scale, st1, row);
+        }
+        fence_proxy_async_smem();   // the TMA engine reads what the threads wrote
+        tc_fence_before();
+        mbar_arrive(&bars->acc_free);
+        mbar_arrive(&bars->epi_staged);
+        bool sok = true;
+        if (threadIdx.x == 128) {
+          if (!mbar_wait(&bars->epi_staged, eli & 1, abort_flag, kWaitBudget)) {
+            sok = false;
+          } else {
+            tma_store_4d(&tmG1, st1, 0, ew.h, ew.row0, ew.b);
+            if (kDkDv) tma_store_4d(&tmG2, st2, 0, ew.h, ew.row0, ew.b);
+            bulk_commit_group();
+            pend_rb = rb;   // released once the stores have read it (next block)
+          }
+        }
+        if (!__all_sync(0xffffffffu, sok)) return false;
+      } else {
+        if (kDkDv) {
+          store_acc_cols<kF32Grad, false, kF16>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg,
+                                          half_cols, 1.0f, row_ptr(p.dv), p.d, store);
+          store_acc_cols<kF32Grad, false, kF16>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg,
+                                          half_cols, p.scale, row_ptr(p.dk), p.d, store);
+        } else {
+          store_acc_cols<kF32Grad, true, kF16>(tmem + lane_base + Cfg::kTAcc2,
+                                         tmem + lane_base + Cfg::kTAcc1, corr, cbeg, half_cols,
+                                         p.scale, row_ptr(p.dq), p.d, store);
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->acc_free);
+        // wide layout, fp32 gradients: the row buffer is free (acc_full)
+        if (kWide && threadIdx.x == 128) mbar_arrive(&bars->r_empty[eli % Cfg::kRBufs]);
+      }
+      return true;
+    };
+    // wide dK/dV kernel: the item whose epilogue is still to run
+    bool epi_pend = false;
+    Item ew_pend{};
+    int eli_pend = 0;
     float L_nx = -INFINITY, D_nx = 0.0f;
     if (!kDkDv) load_row(item_index(0, num_items), L_nx, D_nx);
     // wide dQ kernel: D's first estimate, the float32 dot of this query's dO
@@ -968,6 +1045,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (threadIdx.x == 128) release_rows();
+          // the previous item's deferred epilogue: its accumulators must be
+          // read before this block's P V and dS Q overwrite them
+          if (Cfg::kDefer && t == 0 && epi_pend) {
+            epi_pend = false;
+            if (!epilogue(ew_pend, eli_pend, 0.0f)) {
+              ok = false;
+              break;
+            }
+          }
           // P and dS columns are free once the previous block's accumulating
           // MMAs have completed
           if (nsp >= 2 &&
@@ -1113,70 +1199,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         corr = d_row - d_exact;
         if (g == 0 && grow < N) p.D[hb + grow] = live_row ? d_exact : 0.0f;
       }
-      if (!warp_wait(&bars->acc_full, li & 1, abort_flag, kWaitBudget)) { ok = false; break; }
-      tc_fence_after();
-      const bool store = grow < N;
-      const size_t roff = ((static_cast<size_t>(w.b) * N + (store ? grow : 0)) * H + w.h) *
-                          static_cast<size_t>(p.d);
-      const int half_cols = DP / 2;
-      const int cbeg = g * half_cols;
-      auto row_ptr = [&](void* base) -> void* {
-        return kF32Grad ? static_cast<void*>(static_cast<float*>(base) + roff)
-                        : static_cast<void*>(static_cast<__nv_bfloat16*>(base) + roff);
-      };
-      if constexpr (kWide && !kF32Grad) {
-        // Wide layout, bf16 gradients: stage the rows in this item's row
-        // buffer (its last S/dP MMAs have completed, acc_full says so) and
-        // write them with TMA tensor stores; the buffer is released to the
-        // producer once the stores have read it.
-        const int rb = li % Cfg::kRBufs;
-        uint8_t* st1 = sR1 + rb * Cfg::kRBufBytes;
-        uint8_t* st2 = sR2 + rb * Cfg::kRBufBytes;
-        if (kDkDv) {
-          stage_acc_cols<false, kF16>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg, half_cols, 1.0f,
-                                st1, row);
-          stage_acc_cols<false, kF16>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg, half_cols, p.scale,
-                                st2, row);
-        } else {
-          stage_acc_cols<true, kF16>(tmem + lane_base + Cfg::kTAcc2, tmem + lane_base + Cfg::kTAcc1, corr,
-                               cbeg, half_cols, p.scale, st1, row);
-        }
-        fence_proxy_async_smem();   // the TMA engine reads what the threads wrote
-        tc_fence_before();
-        mbar_arrive(&bars->acc_free);
-        mbar_arrive(&bars->epi_staged);
-        if (threadIdx.x == 128) {
-          if (!mbar_wait(&bars->epi_staged, li & 1, abort_flag, kWaitBudget)) {
-            ok = false;
-          } else {
-            tma_store_4d(&tmG1, st1, 0, w.h, w.row0, w.b);
-            if (kDkDv) tma_store_4d(&tmG2, st2, 0, w.h, w.row0, w.b);
-            bulk_commit_group();
-            pend_rb = rb;   // released once the stores have read it (next block)
-          }
-        }
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-      } else {
-        if (kDkDv) {
-          store_acc_cols<kF32Grad, false, kF16>(tmem + lane_base + Cfg::kTAcc1, 0, 0.0f, cbeg,
-                                          half_cols, 1.0f, row_ptr(p.dv), p.d, store);
-          store_acc_cols<kF32Grad, false, kF16>(tmem + lane_base + Cfg::kTAcc2, 0, 0.0f, cbeg,
-                                          half_cols, p.scale, row_ptr(p.dk), p.d, store);
-        } else {
-          store_acc_cols<kF32Grad, true, kF16>(tmem + lane_base + Cfg::kTAcc2,
-                                         tmem + lane_base + Cfg::kTAcc1, corr, cbeg, half_cols,
-                                         p.scale, row_ptr(p.dq), p.d, store);
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->acc_free);
-        // wide layout, fp32 gradients: the row buffer is free (acc_full)
-        if (kWide && threadIdx.x == 128) mbar_arrive(&bars->r_empty[li % Cfg::kRBufs]);
+      if constexpr (Cfg::kDefer) {
+        epi_pend = true;
+        ew_pend = w;
+        eli_pend = li;
+      } else if (!epilogue(w, li, corr)) {
+        ok = false;
+        break;
       }
       cbase += w.nb;
     }
+    if (ok && Cfg::kDefer && epi_pend && !epilogue(ew_pend, eli_pend, 0.0f)) ok = false;
     if (!ok) raise_abort(bars, p.status);
     // the gradient stores must have completed before the CTA exits
     if (kWide && !kF32Grad && threadIdx.x == 128) {
