@@ -64,7 +64,8 @@
 // C1 tile is made by the element-wise warps in the wide layout (in place over
 // the bf16 tile, once the block's S has read it) and by warp 3 in the narrow
 // one; warps 4-7 and 8-11 are the element-wise warpgroups and the epilogue
-// (each stores half of the columns of the accumulator rows).
+// (each stores half of the columns of the accumulator rows; in the wide dK/dV
+// kernel an item's epilogue runs during the next item's first block).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
