@@ -116,8 +116,6 @@ struct FwdBars {
   uint64_t p_full[kQT];
   uint64_t pv_done[kQT];   // O += P V of a block has completed (separate-P layout)
   uint64_t o_final[kQT];
-  uint64_t stage_free[kQT];   // O staging tile may be overwritten (separate-P layout)
-  uint64_t stage_full[kQT];   // O staging tile written by all 128 threads
   uint64_t drain;
   uint64_t probe;
   uint32_t tmem_base;
@@ -269,8 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->p_full[g], kBM);
       mbar_init(&bars->pv_done[g], 1);
       mbar_init(&bars->o_final[g], 1);
-      mbar_init(&bars->stage_free[g], 1);
-      mbar_init(&bars->stage_full[g], kBM);
     }
     for (int s = 0; s < S; ++s) {
       mbar_init(&bars->k_full[s], 1);
@@ -664,23 +660,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if constexpr (Cfg::kSepP) {
-        // Stage the bf16 O tile in shared memory in the TMA box layout (rows
-        // of 128 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7)), then
-        // one thread stores it with a TMA tensor store (rows >= N and columns
-        // >= d are not written).  The staging tile is reused once the previous
-        // store has read it.
-        // (mbarrier handshakes, so that every wait is bounded)
+        // Each warp stages its 32 bf16 rows of O in shared memory in the TMA
+        // box layout (rows of 128 bytes, 16-byte chunk c of row r at chunk
+        // c ^ (r & 7)) and its lane 0 stores them with one TMA tensor store
+        // (rows >= N and columns >= d are not written): no step waits on
+        // another warp.  Lane 0 issued the warp's previous store of this
+        // staging tile, so it alone waits for that store to have read it.
         uint8_t* stage = sO + g * Cfg::kTileBytes;
-        const int e = oc - 1;   // epilogues of this slot so far
-        if (row == 0) {
-          bulk_wait_read_all();
-          mbar_arrive(&bars->stage_free[g]);
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->stage_free[g], e & 1, abort_flag,
-                                               kWaitBudget))) {
-          ok = false;
-          return false;
-        }
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll
         for (int cc = 0; cc < DP / 32; ++cc) {
           uint32_t orr[32];
@@ -703,18 +691,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         fence_proxy_async_smem();   // the TMA engine reads what the threads wrote
-        mbar_arrive(&bars->stage_full[g]);
-        if (row == 0) {
-          if (!mbar_wait(&bars->stage_full[g], e & 1, abort_flag, kWaitBudget)) {
-            ok = false;
-          } else {
-            tma_store_4d(&tmO, stage, 0, ew.h, eqt * kBM, ew.b);
-            bulk_commit_group();
-          }
-        }
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          return false;
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_4d(&tmO, stage + quarter * 32 * 128, 0, ew.h, eqt * kBM + quarter * 32, ew.b);
+          bulk_commit_group();
         }
       } else {
         __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
@@ -944,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && epi_pend) ok = finish_pending(true);
     if (!ok) raise_abort(bars, p.status);
     // the O stores must have completed (and read shared memory) before exit
-    if (Cfg::kSepP && row == 0) bulk_wait_all();
+    if (Cfg::kSepP && lane == 0) bulk_wait_all();
     __syncwarp();
   };
 
@@ -981,7 +961,7 @@ cudaError_t launch_tc(const FwdParams& p, cudaStream_t st) {
   if (e == cudaSuccess) e = make_bhnd_tmap(&mv, p.v, p.B, p.N, p.H, p.d, kBM, 64, kF16);
   // the split-KV partial pass writes float32 rows directly; its O map is unused
   if (e == cudaSuccess)
-    e = make_bhnd_tmap(&mo, kSplit ? p.q : p.o, p.B, p.N, p.H, p.d, kBM, 64, kF16);
+    e = make_bhnd_tmap(&mo, kSplit ? p.q : p.o, p.B, p.N, p.H, p.d, 32, 64, kF16);
   if (e != cudaSuccess) return e;
   auto kern = fwd_tc_kernel<DP, kCausal, kF16, kSplit>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
