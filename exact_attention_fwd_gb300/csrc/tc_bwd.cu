@@ -1102,15 +1102,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kDkDv) {
           if (kCausal && col0 < w.row0 + kRows - 1) {
             const int lim = grow - col0;   // columns cl < lim are masked
+            // one 32-bit keep mask per 32 columns, a bit select per score
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
-              sr[i] = (i < lim) ? __float_as_uint(-INFINITY) : sr[i];
+            for (int k = 0; k < 2; ++k) {
+              const int sh = lim - 32 * k;   // keep columns 32k + sh ..
+              const uint32_t keep = sh <= 0 ? 0xffffffffu : (sh >= 32 ? 0u : (0xffffffffu << sh));
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                sr[32 * k + i] = ((keep >> i) & 1u) ? sr[32 * k + i] : __float_as_uint(-INFINITY);
+            }
           }
         } else if ((kCausal && col0 + 63 > w.row0) || (col0 + 64 > N)) {
           const int lim = min(kCausal ? grow - col0 : 64, N - 1 - col0);   // cl > lim masked
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            sr[i] = (i > lim) ? __float_as_uint(-INFINITY) : sr[i];
+          for (int k = 0; k < 2; ++k) {
+            const int sh = lim - 32 * k;   // keep columns 32k .. 32k + sh
+            const uint32_t keep =
+                sh >= 31 ? 0xffffffffu : (sh < 0 ? 0u : (0xffffffffu >> (31 - sh)));
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              sr[32 * k + i] = ((keep >> i) & 1u) ? sr[32 * k + i] : __float_as_uint(-INFINITY);
+          }
         }
         // Element-wise math on packed pairs (f32x2): t = s c - L2,
         // P = 2^t, dS = P (dP - D); the dQ kernel also sums P dP per row.

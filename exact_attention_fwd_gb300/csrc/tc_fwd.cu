@@ -790,14 +790,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // Blocks with masked keys (the diagonal block of a causal tile, the
         // ragged last block) set them to -inf before the row max: key k0 + i
-        // is masked when i > lim (beyond N, or after q_row).  One copy of the
-        // row loops serves every block (the instruction cache holds it once).
+        // is masked when i > lim (beyond N, or after q_row).  The limit
+        // becomes one 32-bit keep mask per 32 columns, and each score a
+        // select on one bit of it (cheaper than a compare per score).  One
+        // copy of the row loops serves every block (the instruction cache
+        // holds it once).
         const int jb = w.j0 + j;   // the block's index among the head's keys
         if ((kCausal && jb == qt) || ((jb + 1) * kBN > N)) {
           const int k0 = jb * kBN;
           const int lim = min(N - k0 - 1, kCausal ? q_row - k0 : kBN);
 #pragma unroll
-          for (int i = 0; i < kBN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
+          for (int k = 0; k < kBN / 32; ++k) {
+            const int sh = lim - 32 * k;   // keep columns 32k .. 32k + sh
+            const uint32_t keep =
+                sh >= 31 ? 0xffffffffu : (sh < 0 ? 0u : (0xffffffffu >> (31 - sh)));
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              s[32 * k + i] = ((keep >> i) & 1u) ? s[32 * k + i] : -INFINITY;
+          }
         }
         bool rise = false;
         float alpha = 1.0f;
