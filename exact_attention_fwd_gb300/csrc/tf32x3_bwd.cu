@@ -385,12 +385,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->sp_free);   // S and dP may take the next block's scores
       uint32_t xh[kBlk], xl[kBlk], yh[kBlk], yl[kBlk];
+      // masked pairs: P = 0 (dQ: key beyond N or after the query; dK/dV:
+      // query before the key; queries beyond N carry L2 = +inf), as one keep
+      // bit per column of the block
+      uint32_t keep;
+      if constexpr (kDkDv) {
+        const int sh = kCausal ? grow - col0 : 0;   // keep columns sh ..
+        keep = sh <= 0 ? 0xffffffffu : (sh >= 32 ? 0u : (0xffffffffu << sh));
+      } else {
+        const int lim = (kCausal ? min(grow, N - 1) : N - 1) - col0;   // keep columns .. lim
+        keep = lim >= 31 ? 0xffffffffu : (lim < 0 ? 0u : (0xffffffffu >> (31 - lim)));
+      }
 #pragma unroll
       for (int j = 0; j < kBlk; ++j) {
-        const int col = col0 + j;
-        // masked pairs: P = 0 (dQ: key beyond N or after the query; dK/dV:
-        // query before the key; queries beyond N carry L2 = +inf)
-        const bool masked = kDkDv ? (kCausal && col < grow) : (col >= N || (kCausal && col > grow));
+        const bool masked = ((keep >> j) & 1u) == 0u;
         const float l2 = kDkDv ? l2c[j] : l2_row;
         const float dd = kDkDv ? dc[j] : d_row;
         const float pv = masked ? 0.0f : fast_exp2(__uint_as_float(sr[j]) * c - l2);

@@ -318,8 +318,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k0 = j * kBN;
       if ((kCausal && k0 + kBN - 1 > qt * kBM) || k0 + kBN > N) {
         const int lim = min(N - 1 - k0, kCausal ? q_row - k0 : kBN - 1);
+        // one 32-bit keep mask per 32 columns, a bit select per score
 #pragma unroll
-        for (int i = 0; i < kBN; ++i) t[i] = (i > lim) ? -INFINITY : t[i];
+        for (int k = 0; k < kBN / 32; ++k) {
+          const int sh = lim - 32 * k;   // keep columns 32k .. 32k + sh
+          const uint32_t keep =
+              sh >= 31 ? 0xffffffffu : (sh < 0 ? 0u : (0xffffffffu >> (31 - sh)));
+#pragma unroll
+          for (int i = 0; i < 32; ++i) t[32 * k + i] = ((keep >> i) & 1u) ? t[32 * k + i] : -INFINITY;
+        }
       }
       float m_blk = -INFINITY;
 #pragma unroll
