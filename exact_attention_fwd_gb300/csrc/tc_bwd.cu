@@ -84,7 +84,11 @@ constexpr int kRows = 128;       // rows owned by a work item
 constexpr int kThreads = 384;
 constexpr int kRegsHelper = 88;    // warps 0-3: TMA, MMA, vectors, fp16 copy
 constexpr int kRegsElem = 208;     // warps 4-11: element-wise and epilogue
-static_assert(4 * 32 * kRegsHelper + 8 * 32 * kRegsElem <= 168 * kThreads,
+// Registers move between warps within an SM sub-partition (warps k, k + 4,
+// k + 8: one helper and two element-wise warps), so the split must fit each
+// sub-partition's launch allocation, not only the CTA's.
+static_assert(kRegsHelper + 2 * kRegsElem <= 3 * 168 &&
+                  4 * 32 * kRegsHelper + 8 * 32 * kRegsElem <= 168 * kThreads,
               "register split exceeds the launch allocation");
 constexpr int kTmemCols = 512;
 constexpr int kStagesMax = 4;

@@ -78,7 +78,11 @@ constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 0.0f;
 constexpr int kRegsLoad = 72;            // warps 0-3 (TMA, MMA, Q loads)
 constexpr int kRegsSoftmax = 216;        // warps 4-11
-static_assert(4 * 32 * kRegsLoad + 8 * 32 * kRegsSoftmax <= 168 * kThreads,
+// Registers move between warps within an SM sub-partition (warps k, k + 4,
+// k + 8: one load/MMA warp and two softmax warps), so the split must fit each
+// sub-partition's launch allocation, not only the CTA's.
+static_assert(kRegsLoad + 2 * kRegsSoftmax <= 3 * 168 &&
+                  4 * 32 * kRegsLoad + 8 * 32 * kRegsSoftmax <= 168 * kThreads,
               "register split exceeds the launch allocation");
 
 // TMEM columns.  S_g: [128 g, 128 g + 128).  O_g: [256 + DP g, 256 + DP g + DP).
