@@ -75,6 +75,17 @@ def test_ragged_n_backward_bf16(causal, N):
     compare_bwd(inp, out, causal, default_scale(64), TOL["bf16"]["grad"])
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [160, 193, 287])
+def test_row_quarter_boundaries_backward_bf16(causal, N):
+    """Sequence ends inside a 32-row quarter and inside a 32-column word of
+    the dQ kernel's keep masks, several heads per launch."""
+    require_gpu()
+    inp = make(2, 3, N, 64, "bf16", 9700 + N)
+    out = run_fwd_bwd(inp, causal=causal)
+    compare_bwd(inp, out, causal, default_scale(64), TOL["bf16"]["grad"])
+
+
 @pytest.mark.parametrize("d", [8, 16, 32, 40, 64, 96, 128])
 def test_head_dims_backward_bf16(d):
     require_gpu()

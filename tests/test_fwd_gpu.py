@@ -55,6 +55,19 @@ def test_ragged_n_bf16(causal, N):
     compare_fwd(inp, o, lse, causal, default_scale(64))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [160, 193, 224, 287])
+def test_row_quarter_boundaries_bf16(causal, N):
+    """Sequence ends inside each 32-row quarter of a 128-row tile: each warp
+    stores its own 32 output rows (a box partly or wholly past N), and the
+    keep masks of the ragged and diagonal blocks end inside a 32-column word.
+    Several heads, so that CTAs run more than one item."""
+    require_gpu()
+    inp = make(2, 5, N, 64, "bf16", 6500 + N)
+    o, lse, _ = run_fwd(inp, causal=causal)
+    compare_fwd(inp, o, lse, causal, default_scale(64))
+
+
 @pytest.mark.parametrize("d", [8, 16, 24, 32, 40, 56, 64, 72, 96, 120, 128])
 def test_head_dims_bf16(d):
     require_gpu()
